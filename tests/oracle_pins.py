@@ -1,0 +1,337 @@
+"""Pins that hold the CPU oracle to the report, not to itself.
+
+Each ``pin_*`` function takes the path of a compiled oracle library and
+raises AssertionError when the oracle disagrees with something fixed
+independently of it:
+
+  * hand-computed values of the report's closed forms (tests/golden/),
+  * an independently built [page, 2L, ps, H, D] reference (strided_ref),
+  * the dense per-layer view arithmetic of build_mha_views (view base
+    anchor + b*ps*R plus id*R) against the oracle's envelope offsets,
+  * brute-force invariants on tiny pools (bijection, exact tiling),
+  * round trips (store then gather, move then gather).
+
+Run as a script (``python oracle_pins.py <lib.so>``) it executes every pin
+and exits 1 at the first failure; the mutation test uses that to show each
+planted mistake is caught. Source of every rule: the prhub report on sglang
+PR #34602, "feat(unified-memory): dense KV views for uniform-row MHA/SWA
+models".
+"""
+from __future__ import annotations
+
+import os
+import sys
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+for p in (ROOT, HERE):
+    if p not in sys.path:
+        sys.path.insert(0, p)
+
+import oracle  # noqa: E402
+import strided_ref  # noqa: E402
+import synth  # noqa: E402
+
+GOLDEN = os.path.join(HERE, "golden")
+
+
+def _rows(path):
+    out = []
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                out.append(line.split())
+    return out
+
+
+def _geom(L, H, D, it, ps, P, anchor=0, Dv=None):
+    return oracle.Geometry(L, H, D, it, ps, P, anchor, Dv)
+
+
+def _mk(so, g):
+    return oracle.Oracle(g, so)
+
+
+def _fresh(o: oracle.Oracle, seed=7):
+    n = o.raw_bytes()
+    return synth.sentinel_bytes(seed, 0, n)
+
+
+# ----------------------------------------------------------------- pins
+
+def pin_translate_golden(so):
+    """Hand-computed kernel ids for the tiny pool (tests/golden/translate_tiny.txt)."""
+    o = _mk(so, _geom(2, 2, 8, 2, 4, 64))
+    maps = {
+        "none": None,
+        "tomb1": np.where(np.arange(64) == 1, -1, np.arange(64)).astype(np.int32),
+        "p1to9": np.where(np.arange(64) == 1, 9, np.arange(64)).astype(np.int32),
+    }
+    for slot, case, want in _rows(os.path.join(GOLDEN, "translate_tiny.txt")):
+        ids, err = o.translate(np.array([int(slot)]), maps[case])
+        assert err == 0, (slot, case, err)
+        assert int(ids[0]) == int(want), (slot, case, int(ids[0]), want)
+
+
+def pin_layout_table(so):
+    """Per-workload layout numbers (tests/golden/layout_table.txt)."""
+    for r in _rows(os.path.join(GOLDEN, "layout_table.txt")):
+        L, H, D, it, ps, P = map(int, r[:6])
+        R, pb, tot, tp, nr, lve = map(int, r[7:])
+        s = _mk(so, _geom(L, H, D, it, ps, P)).sizes()
+        got = (s["row_bytes"], s["page_bytes"], s["total"], s["tail_pad"], s["n_rows"], s["last_view_end"])
+        assert got == (R, pb, tot, tp, nr, lve), (r, got)
+
+
+def pin_gates(so):
+    """Start-up gates: uniform rows, anchor alignment, id bound, tail pad."""
+    g = {k: int(v) for k, v in _rows(os.path.join(GOLDEN, "id_bound.txt"))}
+    ok = _mk(so, _geom(80, 1, 64, 1, 256, g["max_pages_ok"]))
+    assert ok.check() == "ok"
+    bad = _mk(so, _geom(80, 1, 64, 1, 256, g["first_pages_rejected"]))
+    assert bad.check() == "id_bound"
+    st = _mk(so, _geom(80, 1, 64, 1, 256, 48828))
+    assert st.sizes()["n_rows"] == g["stress_n_rows"]
+    ids, err = st.translate(np.array([g["stress_last_slot"]]))
+    assert err == 0 and int(ids[0]) == g["stress_last_slot_id"], int(ids[0])
+    # the view-space row of that slot in block 159 is the last row of the view
+    assert int(ids[0]) + 159 * 256 == g["stress_last_row_b159"] == g["stress_n_rows"] - 1
+    assert _mk(so, _geom(1, 1, 16, 1, 2, g["edge_pages_rejected"])).check() == "id_bound"
+    assert _mk(so, _geom(1, 1, 16, 1, 2, g["edge_pages_ok"])).check() == "ok"
+    assert _mk(so, _geom(2, 2, 8, 2, 4, 64, Dv=16)).check() == "asymmetric"
+    assert _mk(so, _geom(2, 2, 8, 2, 4, 64, anchor=3)).check() == "anchor"
+    assert _mk(so, _geom(2, 2, 8, 2, 4, 64, anchor=4)).check() == "ok"
+    t = _mk(so, _geom(2, 2, 8, 2, 4, 64))
+    lve = t.sizes()["last_view_end"]
+    # build_mha_views: the last view ends exactly (2L-1)*ps rows past the pool
+    assert lve == 32768 + 3 * 4 * 32
+    assert t.check(lve) == "ok" and t.check(lve - 1) == "tail_pad"
+    # the pool's own allocation, total + one page envelope, always suffices
+    assert t.check(t.raw_bytes()) == "ok"
+
+
+def pin_bijection(so):
+    """Brute force on tiny pools: (slot, block) -> row is a bijection that tiles
+    the pool exactly, and the oracle's envelope offset of (slot, block) equals
+    the dense view of build_mha_views at row kernel_id(slot): view base
+    anchor + b*ps*R plus kernel_id*R."""
+    for (L, H, D, it, ps, P, anchor) in [
+        (1, 1, 8, 2, 1, 5, 0), (2, 2, 8, 2, 4, 6, 32), (3, 1, 16, 1, 2, 7, 16),
+        (1, 2, 4, 4, 8, 3, 0), (4, 1, 32, 1, 3, 5, 64),
+    ]:
+        o = _mk(so, _geom(L, H, D, it, ps, P, anchor))
+        s = o.sizes()
+        R = s["row_bytes"]
+        slots = np.arange(P * ps, dtype=np.int64)
+        ids, err = o.translate(slots)
+        assert err == 0
+        seen_rows, seen_bytes = [], []
+        for t, kid in zip(slots, ids):
+            for b in range(2 * L):
+                byte = o.slot_row_byte(int(t), b)
+                assert byte == anchor + b * ps * R + int(kid) * R, (t, b, byte)
+                seen_rows.append(int(kid) + b * ps)
+                seen_bytes.append(byte)
+        assert sorted(seen_rows) == list(range(P * 2 * L * ps))
+        assert sorted(seen_bytes) == [anchor + R * k for k in range(s["n_rows"])]
+        assert anchor + R * s["n_rows"] == anchor + s["total"]
+        # ids decode back to the same bytes (the move's decoding)
+        for kid in ids[:: max(1, len(ids) // 17)]:
+            for b in (0, 2 * L - 1):
+                assert o.id_row_byte(int(kid), b) == anchor + b * ps * R + int(kid) * R
+
+
+def _random_case(rng, L, H, D, it, ps, P, anchor, n, tomb):
+    slots = rng.permutation(np.arange(ps, P * ps))[:n].astype(np.int64)
+    if tomb:
+        slots[rng.choice(n, size=tomb, replace=False)] = -1
+    K = synth.kv_values(rng, (n, H, D), it)
+    V = synth.kv_values(rng, (n, H, D), it)
+    return slots, K, V
+
+
+def pin_store_vs_strided(so):
+    """Per-layer and all-layer stores equal the [page, 2L, ps, H, D] reference
+    byte for byte (tombstones included: both write in input order)."""
+    rng = np.random.default_rng(11)
+    for (L, H, D, it, ps, P, anchor, n, tomb) in [
+        (2, 2, 8, 2, 4, 64, 0, 100, 5), (3, 2, 4, 1, 8, 9, 16, 40, 3),
+        (1, 1, 16, 2, 2, 11, 0, 18, 0), (24, 1, 16, 1, 32, 3, 32, 50, 4),
+    ]:
+        o = _mk(so, _geom(L, H, D, it, ps, P, anchor))
+        M = _fresh(o)
+        T = M.copy()
+        env = strided_ref.envelope(T, L, H, D, it, ps, P, anchor)
+        for layer in range(L):
+            slots, K, V = _random_case(rng, L, H, D, it, ps, P, anchor, n, tomb)
+            assert o.store(M, layer, slots, K, V) == 0
+            strided_ref.store(env, layer, slots, K, V)
+            assert np.array_equal(M, T), ("store", L, layer)
+        slots, K, V = _random_case(rng, L, H, D, it, ps, P, anchor, n, tomb)
+        Ka = np.stack([synth.kv_values(rng, (n, H, D), it) for _ in range(L)])
+        Va = np.stack([synth.kv_values(rng, (n, H, D), it) for _ in range(L)])
+        assert o.store_all(M, slots, Ka, Va) == 0
+        for layer in range(L):
+            strided_ref.store(env, layer, slots, Ka[layer], Va[layer])
+        assert np.array_equal(M, T), ("store_all", L)
+
+
+def pin_v2p_store(so):
+    """Virtual->physical page map: store through the map equals the reference
+    store through the same map; tombstoned pages land on the sink."""
+    rng = np.random.default_rng(12)
+    L, H, D, it, ps, P = 2, 2, 8, 2, 4, 16
+    o = _mk(so, _geom(L, H, D, it, ps, P))
+    v2p = (1 + rng.permutation(P - 1)).astype(np.int32)[: P - 1]
+    v2p = np.concatenate([[-1], v2p]).astype(np.int32)  # virtual page 0 -> tombstone
+    v2p[5] = -1
+    slots = rng.permutation(np.arange(0, P * ps))[:30].astype(np.int64)
+    K = synth.kv_values(rng, (30, H, D), it)
+    V = synth.kv_values(rng, (30, H, D), it)
+    M = _fresh(o)
+    T = M.copy()
+    env = strided_ref.envelope(T, L, H, D, it, ps, P)
+    assert o.store(M, 1, slots, K, V, v2p) == 0
+    strided_ref.store(env, 1, slots, K, V, v2p)
+    assert np.array_equal(M, T)
+    ids, err = o.translate(slots, v2p)
+    assert err == 0
+    for t, kid in zip(slots, ids):
+        vp, off = divmod(int(t), ps)
+        if v2p[vp] < 0:
+            assert kid == 0
+        else:
+            assert o.slot_row_byte(int(t), 2, v2p) == (int(kid) + 2 * ps) * H * D * it
+    # a page index past the map is an error and lands on the sink
+    ids, err = o.translate(np.array([P * ps + 1], np.int64), v2p[: P // 2])
+    assert err == oracle.E_V2P and ids[0] == 0
+
+
+def pin_gather_vs_strided(so):
+    """Gather equals the reference read, for full windows, windows starting
+    mid-page, empty sequences and tombstoned (negative) table entries."""
+    rng = np.random.default_rng(13)
+    for (L, H, D, it, ps, P, anchor) in [(2, 2, 8, 2, 4, 64, 0), (3, 1, 32, 1, 8, 13, 48)]:
+        o = _mk(so, _geom(L, H, D, it, ps, P, anchor))
+        M = _fresh(o, seed=99)
+        env = strided_ref.envelope(M, L, H, D, it, ps, P, anchor)
+        S, maxp = 5, 6
+        bt = rng.integers(1, P, size=(S, maxp)).astype(np.int32)
+        bt[2, 1] = -1
+        ln = np.array([maxp * ps, 3, 0, maxp * ps - 5, 2 * ps + 1], np.int32)
+        st = np.array([0, 1, 0, ps + 2, 2 * ps], np.int32)
+        g = synth.GatherBatch(bt, st, ln)
+        for layer in range(L):
+            k, v, err = o.gather(M, layer, bt, ln, g.cu, st)
+            assert err == 0
+            rk, rv = strided_ref.gather(env, layer, bt, st, ln)
+            assert np.array_equal(k, rk.reshape(len(rk), -1).view(np.uint8).reshape(k.shape))
+            assert np.array_equal(v, rv.reshape(len(rv), -1).view(np.uint8).reshape(v.shape))
+
+
+def pin_roundtrip(so):
+    """Store then gather returns the stored rows; move then gather at the
+    destination returns the source rows, and nothing else changes."""
+    rng = np.random.default_rng(14)
+    L, H, D, it, ps, P = 3, 2, 8, 2, 4, 20
+    o = _mk(so, _geom(L, H, D, it, ps, P))
+    R = o.sizes()["row_bytes"]
+    M = _fresh(o)
+    pages = (1 + rng.permutation(P - 1)[:6]).astype(np.int32)
+    bt = pages[None, :]
+    slots = (pages.astype(np.int64)[:, None] * ps + np.arange(ps)).reshape(-1)
+    n = slots.size
+    for layer in range(L):
+        K = synth.kv_values(rng, (n, H, D), it)
+        V = synth.kv_values(rng, (n, H, D), it)
+        assert o.store(M, layer, slots, K, V) == 0
+        g = synth.GatherBatch(bt, np.zeros(1, np.int32), np.array([n], np.int32))
+        k, v, err = o.gather(M, layer, bt, g.seq_len, g.cu, g.seq_start)
+        assert err == 0
+        assert np.array_equal(k, K.reshape(n, -1).view(np.uint8).reshape(n, R))
+        assert np.array_equal(v, V.reshape(n, -1).view(np.uint8).reshape(n, R))
+    # move: tokens of the first two pages -> two fresh pages
+    free = np.setdiff1d(np.arange(1, P), pages)[:2].astype(np.int64)
+    src_slots = slots[: 2 * ps]
+    dst_slots = (free[:, None] * ps + np.arange(ps)).reshape(-1)
+    src_ids, e1 = o.translate(src_slots)
+    dst_ids, e2 = o.translate(dst_slots)
+    before = M.copy()
+    assert o.move(M, src_ids, dst_ids) == 0
+    T = before.copy()
+    strided_ref.move(strided_ref.envelope(T, L, H, D, it, ps, P), src_slots, dst_slots)
+    assert np.array_equal(M, T)
+    btd = free.astype(np.int32)[None, :]
+    bts = pages[:2][None, :]
+    for layer in range(L):
+        g = synth.GatherBatch(btd, np.zeros(1, np.int32), np.array([2 * ps], np.int32))
+        kd, vd, _ = o.gather(M, layer, btd, g.seq_len, g.cu, g.seq_start)
+        ks, vs, _ = o.gather(before, layer, bts, g.seq_len, g.cu, g.seq_start)
+        assert np.array_equal(kd, ks) and np.array_equal(vd, vs)
+    changed = np.nonzero(M != before)[0]
+    dst_bytes = {o.slot_row_byte(int(t), b) for t in dst_slots for b in range(2 * L)}
+    assert all(any(d <= c < d + R for d in dst_bytes) for c in changed[:: max(1, len(changed) // 200)])
+
+
+def pin_tail_untouched(so):
+    """Writing every slot of every layer never touches the anchor prefix or
+    the tail pad (the tail pad exists only so the last view stays in bounds)."""
+    rng = np.random.default_rng(15)
+    L, H, D, it, ps, P, anchor = 2, 1, 16, 2, 4, 5, 64
+    o = _mk(so, _geom(L, H, D, it, ps, P, anchor))
+    s = o.sizes()
+    M = _fresh(o)
+    before = M.copy()
+    slots = np.arange(P * ps, dtype=np.int64)
+    Ka = synth.kv_values(rng, (L, slots.size, H, D), it)
+    Va = synth.kv_values(rng, (L, slots.size, H, D), it)
+    assert o.store_all(M, slots, Ka, Va) == 0
+    assert np.array_equal(M[:anchor], before[:anchor])
+    assert np.array_equal(M[anchor + s["total"] :], before[anchor + s["total"] :])
+    assert np.count_nonzero(M[anchor : anchor + s["total"]] != before[anchor : anchor + s["total"]]) > 0
+
+
+def pin_errors(so):
+    """Error reporting: ids past the pool, ids not in translate form, gather
+    metadata that does not fit the output, and pages past the pool."""
+    L, H, D, it, ps, P = 2, 1, 16, 1, 4, 8
+    o = _mk(so, _geom(L, H, D, it, ps, P))
+    M = _fresh(o)
+    before = M.copy()
+    stride = ps * 2 * L
+    assert o.move(M, np.array([P * stride], np.int32), np.array([stride], np.int32)) == oracle.E_ROW
+    assert o.move(M, np.array([stride + ps], np.int32), np.array([2 * stride], np.int32)) == oracle.E_FORM
+    assert np.array_equal(M, before)
+    ids, err = o.translate(np.array([P * ps], np.int64))
+    assert err == oracle.E_ROW and ids[0] == 0
+    bt = np.array([[1, P]], np.int32)
+    k, v, err = o.gather(M, 0, bt, np.array([2 * ps], np.int32), np.array([0, 2 * ps], np.int64))
+    assert err == oracle.E_ROW
+    k, v, err = o.gather(M, 0, bt[:, :1], np.array([ps], np.int32), np.array([0, ps - 1], np.int64),
+                         out_rows=ps - 1)
+    assert err == oracle.E_TABLE
+
+
+PINS = [
+    pin_translate_golden, pin_layout_table, pin_gates, pin_bijection, pin_store_vs_strided,
+    pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors,
+]
+
+
+def main(argv):
+    so = argv[1]
+    for pin in PINS:
+        try:
+            pin(so)
+        except AssertionError as e:  # a caught mistake
+            print(f"FAILED {pin.__name__}: {e!r}"[:400])
+            return 1
+    print("all pins hold")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main(sys.argv))

@@ -1,0 +1,85 @@
+"""The oracle against its pins, and planted mistakes against the pins.
+
+Every pin in ``oracle_pins`` must hold for the committed oracle. Then each
+mutation below is planted in a copy of kv_oracle.c (on the CPU, in a temp
+directory), compiled, and the whole pin suite is run on it in a child
+process: every mutant must be caught (a failing pin, or a crash).
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+import oracle_pins
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.mark.parametrize("pin", oracle_pins.PINS, ids=lambda f: f.__name__)
+def test_pin_holds(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+# (name, original text, planted mistake)
+MUTANTS = [
+    ("stride_drops_factor_2",
+     "int64_t stride = (int64_t)d->page_size * (2 * (int64_t)d->layer_num);\n    for",
+     "int64_t stride = (int64_t)d->page_size * ((int64_t)d->layer_num);\n    for"),
+    ("tail_pad_one_block_short",
+     "out[4] = (int64_t)d->page_size * (blocks * R);",
+     "out[4] = (int64_t)d->page_size * ((blocks - 1) * R);"),
+    ("envelope_block_offset_transposed",
+     "b * ((int64_t)d->page_size * R) + o * R;",
+     "o * ((int64_t)d->page_size * R) + b * R;"),
+    ("v_written_to_k_block",
+     "memcpy(M + env_byte(d, p, 2 * (int64_t)layer + 1, o), V + i * R, (size_t)R);",
+     "memcpy(M + env_byte(d, p, 2 * (int64_t)layer, o), V + i * R, (size_t)R);"),
+    ("k_and_v_blocks_swapped_in_gather",
+     "memcpy(outK + r * R, M + env_byte(d, p, 2 * (int64_t)layer, o), (size_t)R);",
+     "memcpy(outK + r * R, M + env_byte(d, p, 2 * (int64_t)layer + 1, o), (size_t)R);"),
+    ("gather_output_row_ignores_start",
+     "int64_t r = cu[s] + (j - st);",
+     "int64_t r = cu[s] + j;"),
+    ("gather_offset_from_wrong_operand",
+     "int64_t o = j % ps;",
+     "int64_t o = k % ps;"),
+    ("id_bound_allows_2_pow_31",
+     "int64_t limit = ((int64_t)1 << 31) - 1;",
+     "int64_t limit = ((int64_t)1 << 31);"),
+    ("page_map_ignored",
+     "phys = v2p[page];",
+     "phys = page;"),
+    ("tombstoned_page_not_clamped",
+     "if (phys < 0) return 0;                    /* tombstoned page -> sink */",
+     "if (phys < 0) phys = -phys;"),
+    ("move_copies_half_the_blocks",
+     "for (int64_t b = 0; b < blocks; ++b)\n            memcpy(snap",
+     "for (int64_t b = 0; b < blocks / 2; ++b)\n            memcpy(snap"),
+    ("move_decodes_offset_with_page_size",
+     "*o = id % stride;",
+     "*o = id % d->page_size;"),
+    ("last_view_end_drops_block_reach",
+     "out[6] = d->anchor + (blocks - 1) * d->page_size * R + n_rows * R;",
+     "out[6] = d->anchor + n_rows * R;"),
+    ("layer_stride_one_block",
+     "int64_t page_bytes = (int64_t)d->page_size * blocks * R;",
+     "int64_t page_bytes = (int64_t)d->page_size * (blocks - 1) * R;"),
+    ("asymmetric_not_rejected",
+     "if (d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;",
+     ""),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(name, orig, mut, tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "kv_oracle.c")).read()
+    assert src.count(orig) == 1, f"mutation site for {name} not unique/present"
+    c = tmp_path / "mutant.c"
+    so = tmp_path / "libmutant.so"
+    c.write_text(src.replace(orig, mut))
+    subprocess.check_call(["gcc", "-O1", "-std=c99", "-shared", "-fPIC", str(c), "-o", str(so)])
+    r = subprocess.run([sys.executable, os.path.join(HERE, "oracle_pins.py"), str(so)],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant {name} survived every pin:\n{r.stdout}\n{r.stderr}"
