@@ -1,0 +1,444 @@
+"""Throughput of the page-major KV pool's hot path on one GB300 (or N replicas).
+
+One step is one pass of the whole path on the Llama-3-8B-shaped decode
+workload (L=32 layers, 8 KV heads, head_dim 128, bf16, page size 16, 4096
+pages = an 8 GiB pool):
+  1. kv_translate          512 slots -> ids (256 decode tokens + 256 chunk tokens)
+  2. kv_store_all_layers   the 256-token chunk into all 32 layers (one launch)
+  3. for each of the 32 layers:
+       kv_store_layer      the 256 decode tokens (one per sequence)
+       kv_gather_layer     256 sequences x 4096 context tokens through block tables
+  4. kv_move               8192 tokens (all 64 row-blocks each) to new slots
+Metric: useful GB/s = algorithmic bytes moved per step (every payload row read
+once and written once, plus index bytes) / step time, with inputs resident in
+HBM. The working set (8 GiB pool, 4 GiB of gather output per layer) is far
+larger than L2, so no flush is needed between steps.
+
+`--impl reference` times the CPU oracle (oracle/, plain C loops) on a bounded
+sample of the same step on the host cores, same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+GB = 1e9
+SHAPE = synth.SHAPES[2]
+N_DECODE = 256          # sequences, one new token each
+CTX = 4096              # context tokens per sequence
+N_CHUNK = 256           # tokens of a prefill chunk stored into all layers at once
+N_MOVE = 8192           # tokens moved per step
+WORKLOAD = ("llama3-8b-decode: L=32 H_kv=8 D=128 bf16 ps=16 P=4096 (8 GiB pool); step = translate 512 slots, "
+            "store_all_layers 256 chunk tokens, 32 x (store_layer 256 decode tokens + gather 256 seqs x 4096 "
+            "tokens), move 8192 tokens x 64 row-blocks")
+
+
+def useful_bytes(shape=SHAPE, n_decode=N_DECODE, ctx=CTX, n_chunk=N_CHUNK, n_move=N_MOVE, n_seqs=None):
+    """Algorithmic bytes per step, by kernel (every row read once and written
+    once, plus the index bytes each kernel must read)."""
+    L, R, ps = shape.layer_num, shape.row_bytes, shape.page_size
+    n_seqs = n_decode if n_seqs is None else n_seqs
+    rows = n_seqs * ctx
+    return {
+        "translate": (n_decode + n_chunk) * (8 + 4),
+        "store_all_layers": n_chunk * (2 * L * R * 2 + 4),
+        "store_layer": L * n_decode * (2 * R * 2 + 4),
+        "gather": L * (rows * 4 * R + rows * 4 // ps),
+        "move": n_move * (2 * L * R * 2 + 8),
+    }
+
+
+# ------------------------------------------------------------------ inputs
+
+def make_inputs(rank: int, shape=SHAPE, n_decode=N_DECODE, ctx=CTX, n_chunk=N_CHUNK, n_move=N_MOVE):
+    """Seeded host inputs of one step (numpy)."""
+    ps, P = shape.page_size, shape.num_pages
+    rng = synth.rng_for(shape.seed + 7919 * rank, synth.S_MISC, 0)
+    slots = synth.distinct_slots(rng, ps, P * ps, n_decode + n_chunk + 2 * n_move)
+    dec, chunk = slots[:n_decode], slots[n_decode:n_decode + n_chunk]
+    mv = slots[n_decode + n_chunk:]
+    npg = ctx // ps
+    bt = np.stack([1 + rng.permutation(P - 1)[:npg] for _ in range(n_decode)]).astype(np.int32)
+    g = synth.GatherBatch(bt, np.zeros(n_decode, np.int32), np.full(n_decode, ctx, np.int32))
+    kd, vd = synth.kv_pair(shape, shape.layer_num * n_decode, 0, seed=shape.seed + rank)
+    kc, vc = synth.kv_pair(shape, shape.layer_num * n_chunk, 1, seed=shape.seed + rank)
+    L, R = shape.layer_num, shape.row_bytes
+
+    def rows(a, n):
+        return np.ascontiguousarray(a).view(np.uint8).reshape(L, n, R)
+
+    return dict(slots=np.concatenate([dec, chunk]).astype(np.int64), g=g,
+                k_dec=rows(kd, n_decode), v_dec=rows(vd, n_decode),
+                k_chunk=rows(kc, n_chunk), v_chunk=rows(vc, n_chunk),
+                move_src=mv[:n_move], move_dst=mv[n_move:])
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str | None):
+        self.proc = None
+        self.lines: list[str] = []
+        self.device_id = device_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.device_id:
+            cmd += ["-i", self.device_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ peaks / profile
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def profiled_traffic(kernel_source: str):
+    """DRAM bytes per gather launch from the committed ncu summary, or None when
+    the kernel source changed since the counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "gather_decode_llama3_8b.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    want = hashlib.sha256(open(kernel_source, "rb").read()).hexdigest()[:16]
+    src_hash = traffic = None
+    for line in text.splitlines():
+        if line.startswith("kernel_source_sha256_16:"):
+            src_hash = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_full_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if src_hash == want else None
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(budget_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of the step: a 256-page
+    pool of the same model shape, 16 sequences x 4096 tokens gathered for one
+    layer, the 256-token all-layer store, 256 decode tokens stored for one
+    layer, and 512 moved tokens; repeated until `budget_s` has elapsed."""
+    import oracle as ora
+
+    P = 256
+    sh = SHAPE.scaled(P)
+    o = ora.Oracle(ora.Geometry(sh.layer_num, sh.head_num, sh.head_dim, sh.itemsize, sh.page_size, P))
+    M = synth.sentinel_bytes(5, 0, o.raw_bytes())
+    rng = synth.rng_for(sh.seed, synth.S_MISC, 1)
+    ps = sh.page_size
+    slots = synth.distinct_slots(rng, ps, P * ps, 256 + 256 + 1024)
+    bt = rng.integers(1, P, size=(16, CTX // ps)).astype(np.int32)
+    g = synth.GatherBatch(bt, np.zeros(16, np.int32), np.full(16, CTX, np.int32))
+    kc, vc = synth.kv_pair(sh, sh.layer_num * 256, 1)
+    kd, vd = synth.kv_pair(sh, 256, 0)
+    src, _ = o.translate(slots[512:1024])
+    dst, _ = o.translate(slots[1024:])
+    R = sh.row_bytes
+    outk = np.empty((g.total, R), np.uint8)
+    outv = np.empty((g.total, R), np.uint8)
+    per = useful_bytes(sh, n_decode=256, ctx=CTX, n_chunk=256, n_move=512, n_seqs=16)
+    per_rep = per["translate"] + per["store_all_layers"] + per["store_layer"] // sh.layer_num + \
+        per["gather"] // sh.layer_num + per["move"]
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        o.translate(slots[:512])
+        o.store_all(M, slots[256:512], kc, vc)
+        o.store(M, 5, slots[:256], kd, vd)
+        o.gather(M, 5, g.block_table, g.seq_len, g.cu, g.seq_start, g.total, outk, outv)
+        o.move(M, src, dst)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": per_rep * reps / el / GB, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{reps} reps of: 256-page pool of the same shape; translate 512 slots; store_all 256 "
+                       f"tokens x 32 layers; store_layer 256 tokens; gather 16 seqs x 4096 tokens for one layer; "
+                       f"move 512 tokens; {el:.1f} s single-threaded"),
+            "seconds": el}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import gather_translate_kv_gb300 as gt
+    from gather_translate_kv_gb300 import build as gbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        gbuild.build()
+    if world > 1:
+        dist.barrier()
+    gt.lib()
+
+    sh = SHAPE
+    L, R, ps = sh.layer_num, sh.row_bytes, sh.page_size
+    inp = make_inputs(rank)
+    total, pad = gt.kv_pool_required_bytes(gt.make_desc(L, sh.head_num, sh.head_dim, sh.itemsize, ps,
+                                                        sh.num_pages))
+    raw = torch.empty(total + pad, dtype=torch.uint8, device=dev)
+    synth.fill_sentinel_torch(raw, 17 + rank)
+    pool = gt.kv_pool_create(gt.make_desc(L, sh.head_num, sh.head_dim, sh.itemsize, ps, sh.num_pages), raw)
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    g = inp["g"]
+    dev_in = dict(slots=d(inp["slots"]), bt=d(g.block_table), ln=d(g.seq_len), cu=d(g.cu),
+                  k_dec=d(inp["k_dec"]), v_dec=d(inp["v_dec"]), k_chunk=d(inp["k_chunk"]),
+                  v_chunk=d(inp["v_chunk"]))
+    ids = torch.empty(N_DECODE + N_CHUNK, dtype=torch.int32, device=dev)
+    # move ids are kernel-facing: translate them once with the library
+    mv = torch.empty(2 * N_MOVE, dtype=torch.int32, device=dev)
+    gt.kv_translate(pool, d(np.concatenate([inp["move_src"], inp["move_dst"]])), mv)
+    mv_src, mv_dst = mv[:N_MOVE], mv[N_MOVE:]
+    out_k = torch.empty((g.total, R), dtype=torch.uint8, device=dev)
+    out_v = torch.empty_like(out_k)
+    stream = torch.cuda.current_stream(dev)
+    gather_ev = []
+
+    def step(x, record=False):
+        gt.kv_translate(pool, x["slots"], ids, stream=stream)
+        gt.kv_store_all_layers(pool, ids[N_DECODE:], x["k_chunk"], x["v_chunk"], stream=stream)
+        for layer in range(L):
+            gt.kv_store_layer(pool, layer, ids[:N_DECODE], x["k_dec"][layer], x["v_dec"][layer], stream=stream)
+            if record:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            gt.kv_gather_layer(pool, layer, x["bt"], x["ln"], x["cu"], out_k, out_v, stream=stream)
+            if record:
+                e1.record(stream)
+                gather_ev.append((e0, e1))
+        gt.kv_move(pool, mv_src, mv_dst, stream=stream)
+    launches_per_step = 1 + 1 + 2 * L + 1
+
+    for _ in range(args.warmup):
+        step(dev_in)
+    torch.cuda.synchronize(dev)
+    assert gt.kv_pool_last_error(pool) == 0
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(dev_in, record=True)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    gather_ms = statistics.mean(a.elapsed_time(b) for a, b in gather_ev)
+    dev_err = gt.kv_pool_last_error(pool)
+
+    # end to end: pinned host inputs -> device every step, ids + error word back
+    host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in
+            dict(slots=inp["slots"], bt=g.block_table, ln=g.seq_len, cu=g.cu, k_dec=inp["k_dec"],
+                 v_dec=inp["v_dec"], k_chunk=inp["k_chunk"], v_chunk=inp["v_chunk"]).items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    ids_host = torch.empty(ids.shape, dtype=ids.dtype).pin_memory()
+    d2h = ids_host.numel() * 4 + 4
+    stage = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+
+    def e2e_step():
+        for k, v in host.items():
+            stage[k].copy_(v, non_blocking=True)
+        step(stage)
+        ids_host.copy_(ids, non_blocking=True)
+        return gt.kv_pool_last_error(pool, stream)  # synchronizes: the step's result is on the host
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    e2e_steps = max(3, args.steps // 2)
+    bad = 0
+    for _ in range(e2e_steps):
+        bad |= e2e_step()
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+    ub = useful_bytes()
+    step_bytes = sum(ub.values())
+    ms_t = torch.tensor([ms, e2e_s * 1e3, gather_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms, e2e_ms, gather_ms = ms_t.tolist()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = measured_hbm_peak()
+    gather_bytes = ub["gather"] / L
+    achieved = gather_bytes / (gather_ms * 1e-3) / GB
+    traffic = profiled_traffic(os.path.join(ROOT, "gather_translate_kv_gb300", "csrc", "kv_gather.cu"))
+    line = {
+        "metric": "KV store/gather/move useful GB/s and % of GB300 HBM peak (byte-exact vs oracle)",
+        "value": round(step_bytes * world / (ms * 1e-3) / GB, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8",
+        "data": "synthetic (seeded: bf16 N(0,1) K/V, random block tables and slots)",
+        "config": {"workload": WORKLOAD, "kv_dtype": "bf16", "useful_bytes_per_step": step_bytes,
+                   "useful_bytes_by_kernel": ub, "l2": "no flush: inputs larger than L2 (8 GiB pool, "
+                   "4 GiB gather output per layer)", "parallelism": f"replicas x{world}",
+                   "pct_of_hbm_peak": round(100 * step_bytes / (ms * 1e-3) / GB / peak, 1)},
+        "roofline": {"bound": "hbm", "kernel": "kv_gather_layer", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": gather_bytes, "avg_launch_ms": round(gather_ms, 4)},
+        "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / GB, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "device_errors": dev_err | bad,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(args.cpu_budget)
+        line["cpu_baseline"].pop("seconds", None)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    workload, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(budget / 4)
+    vals = [oracle_sample(budget) for _ in range(args.steps)]
+    v = statistics.mean(x["value"] for x in vals)
+    secs = sum(x["seconds"] for x in vals)
+    line = {
+        "impl": "reference",
+        "metric": "KV store/gather/move useful GB/s and % of GB300 HBM peak (byte-exact vs oracle)",
+        "value": round(v, 3), "unit": "GB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "kv_dtype": "bf16"},
+        "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,247 @@
+// The C ABI of include/kv_pool.h: argument checks, pool bookkeeping and
+// kernel launches. Nothing here touches K/V bytes; every step of the path runs
+// in the kernels of kv_translate.cu, kv_store.cu, kv_gather.cu and kv_move.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <new>
+
+#include "kv_common.cuh"
+#include "kv_layout.h"
+#include "kv_pool.h"
+
+struct kv_pool {
+  kv_pool_desc desc;
+  gtkv::Layout lay;
+  uint8_t* raw;
+  int64_t raw_bytes;
+  int owns_raw;
+  int32_t* d_err;
+  int device;
+  int sm_count;
+  gtkv::DevPool dev;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ps_shift_of(int64_t ps) {
+  if ((ps & (ps - 1)) != 0) return -1;
+  int s = 0;
+  while ((int64_t(1) << s) < ps) ++s;
+  return s;
+}
+
+// Current device must be the pool's.
+int enter(const kv_pool_t* pool) {
+  if (pool == nullptr) return KV_ERR_INVALID;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
+  return dev == pool->device ? KV_OK : KV_ERR_DEVICE;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
+
+cudaStream_t as_stream(kv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* kv_status_string(int status) {
+  switch (status) {
+    case KV_OK: return "KV_OK";
+    case KV_ERR_INVALID: return "KV_ERR_INVALID";
+    case KV_ERR_ASYMMETRIC: return "KV_ERR_ASYMMETRIC";
+    case KV_ERR_ID_BOUND: return "KV_ERR_ID_BOUND";
+    case KV_ERR_TAIL_PAD: return "KV_ERR_TAIL_PAD";
+    case KV_ERR_ALIGN: return "KV_ERR_ALIGN";
+    case KV_ERR_CUDA: return "KV_ERR_CUDA";
+    case KV_ERR_DEVICE: return "KV_ERR_DEVICE";
+    default: return "KV_ERR_UNKNOWN";
+  }
+}
+
+int kv_pool_required_bytes(const kv_pool_desc* desc, int64_t* total_bytes, int64_t* tail_pad_bytes) {
+  gtkv::Layout lay;
+  const int rc = gtkv::compute_layout(desc, &lay);
+  if (rc != KV_OK) return rc;
+  if (total_bytes) *total_bytes = lay.total;
+  if (tail_pad_bytes) *tail_pad_bytes = lay.tail_pad;
+  return KV_OK;
+}
+
+int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, kv_pool_t** out) {
+  if (out == nullptr) return KV_ERR_INVALID;
+  *out = nullptr;
+  gtkv::Layout lay;
+  int rc = gtkv::compute_layout(desc, &lay);
+  if (rc != KV_OK) return rc;
+  if (raw_dev != nullptr) {
+    if (!aligned16(raw_dev)) return KV_ERR_ALIGN;
+    // build_mha_views: the last view must end inside the raw buffer.
+    if (raw_bytes < lay.last_view_end) return KV_ERR_TAIL_PAD;
+  }
+
+  int dev = -1, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return KV_ERR_CUDA;
+
+  kv_pool* p = new (std::nothrow) kv_pool{};
+  if (p == nullptr) return KV_ERR_INVALID;
+  p->desc = *desc;
+  p->lay = lay;
+  p->device = dev;
+  p->sm_count = sms;
+  if (raw_dev == nullptr) {
+    void* mem = nullptr;
+    if (cudaMalloc(&mem, static_cast<size_t>(lay.alloc_bytes)) != cudaSuccess) {
+      delete p;
+      return KV_ERR_CUDA;
+    }
+    p->raw = static_cast<uint8_t*>(mem);
+    p->raw_bytes = lay.alloc_bytes;
+    p->owns_raw = 1;
+  } else {
+    p->raw = static_cast<uint8_t*>(raw_dev);
+    p->raw_bytes = raw_bytes;
+    p->owns_raw = 0;
+  }
+  void* err = nullptr;
+  if (cudaMalloc(&err, sizeof(int32_t)) != cudaSuccess || cudaMemset(err, 0, sizeof(int32_t)) != cudaSuccess) {
+    if (err) cudaFree(err);
+    if (p->owns_raw) cudaFree(p->raw);
+    delete p;
+    return KV_ERR_CUDA;
+  }
+  p->d_err = static_cast<int32_t*>(err);
+
+  gtkv::DevPool& d = p->dev;
+  d.base = reinterpret_cast<uint4*>(p->raw + desc->anchor_bytes);
+  d.vpr = lay.R / 16;
+  d.ps = desc->page_size;
+  d.stride = lay.stride;
+  d.n_rows = lay.n_rows;
+  d.num_pages = desc->num_pages;
+  d.blocks = static_cast<int32_t>(lay.blocks);
+  d.ps_shift = ps_shift_of(desc->page_size);
+  d.err = p->d_err;
+  *out = p;
+  return KV_OK;
+}
+
+int kv_pool_destroy(kv_pool_t* pool) {
+  if (pool == nullptr) return KV_OK;
+  int rc = KV_OK;
+  if (cudaFree(pool->d_err) != cudaSuccess) rc = KV_ERR_CUDA;
+  if (pool->owns_raw && cudaFree(pool->raw) != cudaSuccess) rc = KV_ERR_CUDA;
+  delete pool;
+  return rc;
+}
+
+int kv_pool_info(const kv_pool_t* pool, kv_pool_info_t* out) {
+  if (pool == nullptr || out == nullptr) return KV_ERR_INVALID;
+  out->raw_dev = pool->raw;
+  out->raw_bytes = pool->raw_bytes;
+  out->row_bytes = pool->lay.R;
+  out->page_bytes = pool->lay.page_bytes;
+  out->total_bytes = pool->lay.total;
+  out->tail_pad_bytes = pool->lay.tail_pad;
+  out->n_rows = pool->lay.n_rows;
+  out->last_view_end = pool->lay.last_view_end;
+  out->device = pool->device;
+  out->owns_raw = pool->owns_raw;
+  return KV_OK;
+}
+
+int kv_translate(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int32_t* v2p_dev,
+                 int64_t v2p_len, int32_t* ids_dev, kv_stream_t stream) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (n < 0 || v2p_len < 0) return KV_ERR_INVALID;
+  if (n == 0) return KV_OK;
+  if (slots_dev == nullptr || ids_dev == nullptr || (v2p_dev == nullptr && v2p_len > 0)) return KV_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(slots_dev) & 7u) || (reinterpret_cast<uintptr_t>(ids_dev) & 3u))
+    return KV_ERR_ALIGN;
+  // ids (int32) must not overlap slots (int64): no in-place translation.
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(slots_dev), s1 = s0 + 8 * static_cast<uintptr_t>(n);
+  const uintptr_t i0 = reinterpret_cast<uintptr_t>(ids_dev), i1 = i0 + 4 * static_cast<uintptr_t>(n);
+  if (i0 < s1 && s0 < i1) return KV_ERR_INVALID;
+  return launched(gtkv::launch_translate(pool->dev, slots_dev, n, v2p_dev, v2p_len, ids_dev, pool->sm_count,
+                                         as_stream(stream)));
+}
+
+int kv_store_layer(const kv_pool_t* pool, int32_t layer, const int32_t* ids_dev, int64_t n, const void* k_dev,
+                   const void* v_dev, kv_stream_t stream) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (n < 0 || layer < 0 || layer >= pool->desc.layer_num) return KV_ERR_INVALID;
+  if (n == 0) return KV_OK;
+  if (ids_dev == nullptr || k_dev == nullptr || v_dev == nullptr) return KV_ERR_INVALID;
+  if (!aligned16(k_dev) || !aligned16(v_dev) || (reinterpret_cast<uintptr_t>(ids_dev) & 3u)) return KV_ERR_ALIGN;
+  return launched(gtkv::launch_store(pool->dev, layer, 1, ids_dev, n, k_dev, v_dev, pool->sm_count,
+                                     as_stream(stream)));
+}
+
+int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n, const void* k_all_dev,
+                        const void* v_all_dev, kv_stream_t stream) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (n < 0) return KV_ERR_INVALID;
+  if (n == 0) return KV_OK;
+  if (ids_dev == nullptr || k_all_dev == nullptr || v_all_dev == nullptr) return KV_ERR_INVALID;
+  if (!aligned16(k_all_dev) || !aligned16(v_all_dev) || (reinterpret_cast<uintptr_t>(ids_dev) & 3u))
+    return KV_ERR_ALIGN;
+  return launched(gtkv::launch_store(pool->dev, 0, pool->desc.layer_num, ids_dev, n, k_all_dev, v_all_dev,
+                                     pool->sm_count, as_stream(stream)));
+}
+
+int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_table_dev, int32_t n_seqs,
+                    int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
+                    const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
+                    kv_stream_t stream) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (layer < 0 || layer >= pool->desc.layer_num || n_seqs < 0 || max_pages < 0 || out_rows < 0)
+    return KV_ERR_INVALID;
+  if (n_seqs == 0) return KV_OK;
+  if (seq_len_dev == nullptr || cu_out_dev == nullptr || (block_table_dev == nullptr && max_pages > 0))
+    return KV_ERR_INVALID;
+  if (out_rows > 0 && (out_k_dev == nullptr || out_v_dev == nullptr)) return KV_ERR_INVALID;
+  if ((out_k_dev && !aligned16(out_k_dev)) || (out_v_dev && !aligned16(out_v_dev)) ||
+      (reinterpret_cast<uintptr_t>(cu_out_dev) & 7u) || (reinterpret_cast<uintptr_t>(seq_len_dev) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_start_dev) & 3u))
+    return KV_ERR_ALIGN;
+  return launched(gtkv::launch_gather(pool->dev, layer, block_table_dev, n_seqs, max_pages, seq_start_dev,
+                                      seq_len_dev, cu_out_dev, out_k_dev, out_v_dev, out_rows, pool->sm_count,
+                                      as_stream(stream)));
+}
+
+int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* dst_ids_dev, int64_t n,
+            kv_stream_t stream) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (n < 0) return KV_ERR_INVALID;
+  if (n == 0) return KV_OK;
+  if (src_ids_dev == nullptr || dst_ids_dev == nullptr) return KV_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(src_ids_dev) & 3u) || (reinterpret_cast<uintptr_t>(dst_ids_dev) & 3u))
+    return KV_ERR_ALIGN;
+  return launched(gtkv::launch_move(pool->dev, src_ids_dev, dst_ids_dev, n, pool->sm_count, as_stream(stream)));
+}
+
+int kv_pool_last_error(const kv_pool_t* pool, kv_stream_t stream, int32_t* dev_code) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (dev_code == nullptr) return KV_ERR_INVALID;
+  int32_t h = 0;
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemcpyAsync(&h, pool->d_err, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaMemsetAsync(pool->d_err, 0, sizeof(int32_t), s) != cudaSuccess) return KV_ERR_CUDA;
+  *dev_code = h;
+  return KV_OK;
+}
+
+}  // extern "C"

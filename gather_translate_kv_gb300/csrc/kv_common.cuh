@@ -1,0 +1,192 @@
+// Shared device-side pieces of the page-major KV pool kernels (sm_103a).
+//
+// Every kernel here is a row mover: a row is R = H*D*itemsize bytes (one
+// token's K or V for one layer), copied as R/16 16-byte vectors. G lanes of a
+// warp cooperate on one row (G = min(32, R/16) for the common power-of-two
+// rows), each lane holding VPL vectors of it; a warp thus covers 32/G rows
+// per wave, and U waves are loaded into registers before any is stored so
+// that every lane keeps several 16-byte loads in flight. All byte offsets are
+// 64-bit: a pool reaches 1.3e11 bytes while ids stay below 2^31.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kv_layout.h"
+#include "kv_pool.h"
+
+namespace gtkv {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kBlock = 256;  // threads per block for every row-moving kernel
+
+// Device view of a pool, passed by value to every kernel.
+struct DevPool {
+  uint4* base;        // raw + anchor (16-byte aligned)
+  int64_t vpr;        // 16-byte vectors per row, R / 16
+  int64_t ps;         // page size
+  int64_t stride;     // rows per page envelope, ps * 2L
+  int64_t n_rows;     // num_pages * 2L * ps
+  int64_t num_pages;  // P
+  int32_t blocks;     // 2L
+  int32_t ps_shift;   // log2(ps) when ps is a power of two, else -1
+  int32_t* err;       // device error word (KV_DEV_ERR_* bits)
+};
+
+__device__ __forceinline__ int64_t div_ps(const DevPool& p, int64_t j) {
+  return p.ps_shift >= 0 ? (j >> p.ps_shift) : j / p.ps;
+}
+
+// ---- 16-byte loads / stores with explicit cache behaviour ---------------
+
+enum : int {
+  kLdNc = 0,     // read-only for the whole kernel: non-coherent path, no L1 allocation
+  kLdPlain = 1,  // buffer is also written by the kernel (move): coherent load, no L1 allocation
+};
+enum : int {
+  kStPlain = 0,   // write-back store
+  kStStream = 1,  // evict-first store for outputs the kernel never reads back
+};
+
+template <int LD>
+__device__ __forceinline__ uint4 ld16(const uint4* p) {
+  uint4 v;
+  if constexpr (LD == kLdNc) {
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+  } else {
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+  }
+  return v;
+}
+
+template <int ST>
+__device__ __forceinline__ void st16(uint4* p, const uint4& v) {
+  if constexpr (ST == kStStream) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  } else {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+}
+
+// ---- copy N rows, all loads before all stores ------------------------------
+//
+// src[i]/dst[i] point at the first vector of row i (not yet offset by the
+// lane); go[i] says whether row i is copied. With VPL > 0 the row holds
+// exactly G*VPL vectors and lane g copies vectors g, g+G, ...; with VPL == 0
+// (rows of any other size, G == 32) the row has vpr vectors and is copied in
+// chunks of 4 vectors per lane.
+template <int G, int VPL, int N, int LD, int ST>
+__device__ __forceinline__ void copy_rows(const uint4* const (&src)[N], uint4* const (&dst)[N],
+                                          const bool (&go)[N], int g, int64_t vpr) {
+  if constexpr (VPL > 0) {
+    uint4 buf[N][VPL];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (go[i]) {
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) buf[i][v] = ld16<LD>(src[i] + g + v * G);
+      }
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (go[i]) {
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) st16<ST>(dst[i] + g + v * G, buf[i][v]);
+      }
+  } else {
+    static_assert(G == 32, "dynamic rows use whole warps");
+#pragma unroll 1
+    for (int i = 0; i < N; ++i) {
+      if (!go[i]) continue;
+#pragma unroll 1
+      for (int64_t c0 = 0; c0 < vpr; c0 += 4 * 32) {
+        uint4 buf[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int64_t c = c0 + g + 32 * k;
+          if (c < vpr) buf[k] = ld16<LD>(src[i] + c);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int64_t c = c0 + g + 32 * k;
+          if (c < vpr) st16<ST>(dst[i] + c, buf[k]);
+        }
+      }
+    }
+  }
+}
+
+// Row geometry chosen on the host from R/16; the list of instantiations.
+enum class RowKind { V4, V8, V16, V32, V64, V128, V256, Dyn };
+
+inline RowKind row_kind(int64_t vpr) {
+  switch (vpr) {
+    case 4: return RowKind::V4;
+    case 8: return RowKind::V8;
+    case 16: return RowKind::V16;
+    case 32: return RowKind::V32;
+    case 64: return RowKind::V64;
+    case 128: return RowKind::V128;
+    case 256: return RowKind::V256;
+    default: return RowKind::Dyn;
+  }
+}
+
+// Calls f.template operator()<G, VPL>() for the row kind.
+template <class F>
+inline cudaError_t dispatch_row(int64_t vpr, F&& f) {
+  switch (row_kind(vpr)) {
+    case RowKind::V4: return f.template operator()<4, 1>();
+    case RowKind::V8: return f.template operator()<8, 1>();
+    case RowKind::V16: return f.template operator()<16, 1>();
+    case RowKind::V32: return f.template operator()<32, 1>();
+    case RowKind::V64: return f.template operator()<32, 2>();
+    case RowKind::V128: return f.template operator()<32, 4>();
+    case RowKind::V256: return f.template operator()<32, 8>();
+    default: return f.template operator()<32, 0>();
+  }
+}
+
+// Blocks per SM a kernel reaches at kBlock threads (cached per instantiation).
+template <class K>
+inline int blocks_per_sm(K kernel) {
+  static int cached = 0;
+  if (cached == 0) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kBlock, 0) != cudaSuccess || nb < 1) nb = 1;
+    cached = nb;
+  }
+  return cached;
+}
+
+// Grid for `warps_needed` warps of work, capped at one full wave of resident
+// blocks (the kernels loop grid-stride over the rest).
+template <class K>
+inline unsigned grid_for(K kernel, int64_t warps_needed, int sm_count) {
+  const int64_t per_block = kBlock / 32;
+  int64_t blocks = (warps_needed + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(sm_count) * blocks_per_sm(kernel);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<unsigned>(blocks);
+}
+
+// ---- launchers (one translation unit each) --------------------------------
+
+cudaError_t launch_translate(const DevPool& p, const int64_t* slots, int64_t n, const int32_t* v2p,
+                             int64_t v2p_len, int32_t* ids, int sm_count, cudaStream_t s);
+cudaError_t launch_store(const DevPool& p, int32_t layer0, int32_t n_layers, const int32_t* ids, int64_t n,
+                         const void* k, const void* v, int sm_count, cudaStream_t s);
+cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
+                          const int32_t* seq_start, const int32_t* seq_len, const int64_t* cu, void* out_k,
+                          void* out_v, int64_t out_rows, int sm_count, cudaStream_t s);
+cudaError_t launch_move(const DevPool& p, const int32_t* src, const int32_t* dst, int64_t n, int sm_count,
+                        cudaStream_t s);
+
+}  // namespace gtkv

@@ -1,0 +1,236 @@
+/*
+ * kv_pool.h -- C ABI of a unified page-major KV-cache pool for uniform-row
+ * MHA / sliding-window attention models, with hand-written CUDA kernels for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Source of the layout and of every operation: the prhub report on sglang PR
+ * #34602, "feat(unified-memory): dense KV views for uniform-row MHA/SWA
+ * models" (cited below as "the report", by section).
+ *
+ * Layout (实现拆解 step 1; 关键源码片段 layout/page_major.py build_mha_views).
+ * One raw byte buffer holds [anchor | pool | tail pad]. The pool is num_pages
+ * page envelopes; each envelope is 2L equal row-blocks of page_size rows,
+ * [L0_K | L0_V | L1_K | L1_V | ...], so layer l's K is block 2l and its V is
+ * block 2l+1. A row is R = head_num * head_dim * itemsize bytes (one token's
+ * K, or V, for one layer). A token slot t (physical page t/ps, offset t%ps)
+ * has the kernel-facing id
+ *
+ *      kernel_id(t) = (t / ps) * (ps * 2L) + t % ps
+ *
+ * and block b of that token is the row at byte
+ *
+ *      anchor + (kernel_id + b * ps) * R.
+ *
+ * Sizes: page_bytes = ps * 2L * R, total = num_pages * page_bytes,
+ * tail_pad = ps * 2L * R (one page envelope: MHASubPoolSpec.
+ * view_tail_pad_bytes returns page_size * entry_bytes, entry_bytes read as
+ * 2L * R), n_rows = num_pages * 2L * ps (kernel-facing rows, must be < 2^31:
+ * _assert_kernel_id_bound, 实现拆解 step 2 and 风险与影响 item 5).
+ *
+ * Conventions for every call below.
+ *  - Pointers named *_dev are device memory of the pool's device; the others
+ *    are host memory. Nothing is retained after a call returns: the caller
+ *    owns every buffer it passes.
+ *  - Compute calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream), launch only this library's kernels, allocate
+ *    nothing and never synchronize, so they can be captured in a CUDA graph.
+ *    kv_pool_last_error is the one call that synchronizes.
+ *  - The calling thread's current device must be the pool's device.
+ *  - Return value: KV_OK (0) or a negative KV_ERR_* code. These are argument,
+ *    layout and launch errors, found on the host before anything is enqueued
+ *    (KV_ERR_CUDA also covers a failed launch).
+ *  - Data-dependent errors (an id, page or table entry pointing outside the
+ *    pool) are never a trap: the kernel skips that row and ORs a
+ *    KV_DEV_ERR_* bit into the pool's device error word, which
+ *    kv_pool_last_error returns and clears.
+ *  - K/V bytes are opaque: no call converts, rounds or inspects them.
+ */
+#ifndef GATHER_TRANSLATE_KV_GB300_KV_POOL_H
+#define GATHER_TRANSLATE_KV_GB300_KV_POOL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host status codes. */
+enum {
+  KV_OK = 0,
+  KV_ERR_INVALID = -1,    /* bad argument: null pointer, negative count, layer out of range */
+  KV_ERR_ASYMMETRIC = -2, /* head_dim != v_head_dim: no uniform row-block array exists */
+  KV_ERR_ID_BOUND = -3,   /* num_pages * 2L * page_size >= 2^31 */
+  KV_ERR_TAIL_PAD = -4,   /* raw buffer ends before the last view does */
+  KV_ERR_ALIGN = -5,      /* a pointer, the anchor or the row size breaks 16-byte alignment */
+  KV_ERR_CUDA = -6,       /* a CUDA runtime call or a kernel launch failed */
+  KV_ERR_DEVICE = -7      /* called with a current device other than the pool's */
+};
+
+/* Bits of the device error word (kv_pool_last_error). */
+#define KV_DEV_ERR_ROW 1   /* an id / page addressed a row outside the pool; row skipped   */
+#define KV_DEV_ERR_V2P 2   /* translate: a virtual page index was past the page map        */
+#define KV_DEV_ERR_TABLE 4 /* gather: sequence metadata inconsistent (see kv_gather_layer) */
+#define KV_DEV_ERR_FORM 8  /* move: an id was not p * ps * 2L + o with o < ps; pair skipped */
+
+typedef struct kv_pool kv_pool_t; /* opaque, host-side, owned by the library */
+
+/* A cudaStream_t without requiring the CUDA headers. */
+typedef struct CUstream_st* kv_stream_t;
+
+/* Pool geometry in the report's notation (build_mha_views' arguments). */
+typedef struct {
+  int32_t layer_num;    /* L >= 1                                                  */
+  int32_t head_num;     /* H >= 1, KV heads                                        */
+  int32_t head_dim;     /* D >= 1                                                  */
+  int32_t v_head_dim;   /* must equal head_dim                                     */
+  int32_t itemsize;     /* bytes per element: 1 (fp8), 2 (bf16/fp16) or 4          */
+  int32_t page_size;    /* ps >= 1 tokens per page                                 */
+  int64_t num_pages;    /* P >= 1; page 0 is the tombstone sink                    */
+  int64_t anchor_bytes; /* byte offset of the pool in the raw buffer, % 16 == 0    */
+} kv_pool_desc;
+
+/* Derived layout of a pool (kv_pool_info). */
+typedef struct {
+  void* raw_dev;         /* start of the raw buffer                       */
+  int64_t raw_bytes;     /* its size                                      */
+  int64_t row_bytes;     /* R                                             */
+  int64_t page_bytes;    /* ps * 2L * R                                   */
+  int64_t total_bytes;   /* num_pages * page_bytes                        */
+  int64_t tail_pad_bytes;/* ps * 2L * R                                   */
+  int64_t n_rows;        /* num_pages * 2L * ps                           */
+  int64_t last_view_end; /* anchor + (2L-1)*ps*R + n_rows*R               */
+  int32_t device;        /* CUDA device ordinal the pool lives on         */
+  int32_t owns_raw;      /* 1 when kv_pool_create allocated the buffer    */
+} kv_pool_info_t;
+
+/* Sizes of a pool, host only, no CUDA call.
+ * Source: UnifiedKVPool.__init__ allocates total_bytes + view_tail_pad_bytes
+ * (关键源码片段 unified_memory_pool.py); page_bytes and n_rows from
+ * build_mha_views (关键源码片段 page_major.py).
+ * Writes *total_bytes = num_pages * ps * 2L * R and *tail_pad_bytes =
+ * ps * 2L * R; the raw buffer a caller allocates is anchor_bytes +
+ * total_bytes + tail_pad_bytes. Either output may be NULL. Runs every gate of
+ * kv_pool_create except the buffer-size one and returns its code. */
+int kv_pool_required_bytes(const kv_pool_desc* desc, int64_t* total_bytes, int64_t* tail_pad_bytes);
+
+/* Create a pool on the current device.
+ * Source: UnifiedKVPool.__init__ and build_mha_views (关键源码片段) with the
+ * start-up gates of 实现拆解 step 2: uniform rows (KV_ERR_ASYMMETRIC), the
+ * kernel-facing id bound (KV_ERR_ID_BOUND), and the last view fitting in the
+ * raw buffer (KV_ERR_TAIL_PAD).
+ *  raw_dev == NULL: the library allocates anchor + total + tail_pad bytes
+ *    (cudaMalloc, contents undefined) and frees them in kv_pool_destroy.
+ *  raw_dev != NULL: the pool borrows the caller's buffer (16-byte aligned,
+ *    raw_bytes long) for its whole life; raw_bytes must reach
+ *    last_view_end = anchor + (2L-1)*ps*R + n_rows*R, which build_mha_views
+ *    asserts, else KV_ERR_TAIL_PAD. A buffer of anchor + total + tail_pad
+ *    bytes always suffices.
+ * Additionally requires R % 16 == 0 and anchor_bytes % 16 == 0
+ * (KV_ERR_ALIGN): every kernel moves rows as 16-byte vectors.
+ * Also allocates a 4-byte device error word. Launches no kernel.
+ * On success *out receives the handle; on failure *out is set to NULL and
+ * nothing stays allocated. */
+int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, kv_pool_t** out);
+
+/* Free a pool: the error word, and the raw buffer if the library allocated
+ * it. Synchronizes nothing; the caller must ensure no work using the pool is
+ * still in flight. NULL is accepted. */
+int kv_pool_destroy(kv_pool_t* pool);
+
+/* Copy the derived layout of a pool into *out (host only). */
+int kv_pool_info(const kv_pool_t* pool, kv_pool_info_t* out);
+
+/* Token slots -> kernel-facing int32 ids.
+ * Source: MultiEndedAllocator.translate_kv_loc_for_kernel (关键源码片段
+ * multi_ended_allocator.py; 实现拆解 step 3): page = t / ps, off = t % ps,
+ * phys = v2p[page] when a page map is given (else phys = page),
+ * id = phys * (ps * 2L) + off, clamped to 0 (the page-0 sink) when t < 0 or
+ * phys < 0. kernel_page_multiplier is always blocks_per_page() = 2L.
+ *  slots_dev  int64 [n]
+ *  v2p_dev    int32 [v2p_len] virtual -> physical page map, or NULL
+ *  ids_dev    int32 [n] output; must not overlap slots_dev (the report's
+ *             in-place aliasing case is not supported)
+ * Device errors: a page index >= v2p_len sets KV_DEV_ERR_V2P, a physical page
+ * >= num_pages sets KV_DEV_ERR_ROW; both write id 0. n == 0 is a no-op. */
+int kv_translate(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int32_t* v2p_dev,
+                 int64_t v2p_len, int32_t* ids_dev, kv_stream_t stream);
+
+/* Per-layer store: row i of K goes to block 2*layer and row i of V to block
+ * 2*layer+1 of token ids_dev[i], i.e. bytes anchor + (id + 2*layer*ps) * R and
+ * anchor + (id + (2*layer+1)*ps) * R.
+ * Source: _store_kv_layer's plain 3D assignment through the dense per-layer
+ * views k_buffer[l][ids] = k, v_buffer[l][ids] = v (关键文件 memory_pool.py
+ * and cache_move.py; build_mha_views' view bases).
+ *  ids_dev  int32 [n] kernel-facing ids (kv_translate's output)
+ *  k_dev    [n, H, D] contiguous, R bytes per row, 16-byte aligned
+ *  v_dev    [n, H, D] contiguous, R bytes per row, 16-byte aligned
+ * Duplicate ids (tombstones all map to id 0, the sink) leave the row with
+ * some mix of the duplicates' words: which one wins is unspecified.
+ * Device errors: an id outside [0, n_rows) sets KV_DEV_ERR_ROW; its rows are
+ * skipped. */
+int kv_store_layer(const kv_pool_t* pool, int32_t layer, const int32_t* ids_dev, int64_t n,
+                   const void* k_dev, const void* v_dev, kv_stream_t stream);
+
+/* All-layer store: kv_store_layer for every layer l in one launch, with
+ * K_all[l] and V_all[l] as layer l's rows.
+ * Source: the same assignment as kv_store_layer, over all 2L row-blocks of
+ * the envelope (实现拆解 step 1).
+ *  k_all_dev, v_all_dev  [L, n, H, D] contiguous (layer-major), 16-byte aligned */
+int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n, const void* k_all_dev,
+                        const void* v_all_dev, kv_stream_t stream);
+
+/* Block-table gather of one layer into packed K and V outputs.
+ * Source: the read path the report describes -- each layer's K/V read
+ * "through one contiguous tensor and one shared block table" (功能与动机) --
+ * over build_mha_views' dense views.
+ * For sequence s and every token j in [start_s, len_s):
+ *    p = block_table[s * max_pages + j / ps]   (a physical page)
+ *    o = j % ps; if p < 0 the token reads the sink (p = 0, o = 0)
+ *    out_k[cu_out[s] + j - start_s] = K row of (p, o) for `layer`
+ *    out_v[cu_out[s] + j - start_s] = V row of (p, o) for `layer`
+ *  block_table_dev int32 [n_seqs, max_pages]
+ *  seq_start_dev   int32 [n_seqs] first token of each window, or NULL for 0
+ *  seq_len_dev     int32 [n_seqs] one past the last token
+ *  cu_out_dev      int64 [n_seqs + 1] output row of each sequence's first
+ *                  token; non-decreasing, cu_out[0] >= 0, and
+ *                  cu_out[s+1] - cu_out[s] >= len_s - start_s
+ *  out_k_dev, out_v_dev  [out_rows, H, D], 16-byte aligned
+ * Output rows not covered by a token (gaps between sequences) are left
+ * untouched. The kernel reads the row count cu_out[n_seqs] on the device, so
+ * the call needs no host synchronization.
+ * Device errors: KV_DEV_ERR_TABLE when some sequence has start_s < 0,
+ * len_s > max_pages * ps, cu_out[s] < 0, cu_out[s+1] < cu_out[s] or a span
+ * shorter than its token count, or when cu_out[n_seqs] > out_rows (rows past
+ * out_rows are not written); KV_DEV_ERR_ROW when a page is >= num_pages (that
+ * token is skipped). Every access stays in bounds whatever the metadata. */
+int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_table_dev, int32_t n_seqs,
+                    int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
+                    const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
+                    kv_stream_t stream);
+
+/* Move: copy every row-block (all layers' K and V, 2L rows) of token
+ * src_ids[i] to token dst_ids[i].
+ * Source: move_kv_cache / _move_kv_cache_impl (关键文件 memory_pool.py).
+ *  src_ids_dev, dst_ids_dev  int32 [n] kernel-facing ids
+ * Precondition: the src set and the dst set are disjoint and dst ids are
+ * distinct; otherwise the result is unspecified (still in bounds).
+ * Device errors: an id outside [0, n_rows) sets KV_DEV_ERR_ROW and an id
+ * whose offset id % (ps*2L) is >= ps sets KV_DEV_ERR_FORM; that pair is
+ * skipped. */
+int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* dst_ids_dev, int64_t n,
+            kv_stream_t stream);
+
+/* Read and clear the pool's device error word. Synchronizes `stream`, then
+ * writes the KV_DEV_ERR_* bits raised since the last read into *dev_code and
+ * zeroes the word (ordered on `stream`). Errors raised by work still running
+ * on other streams may show up in a later read. */
+int kv_pool_last_error(const kv_pool_t* pool, kv_stream_t stream, int32_t* dev_code);
+
+/* Name of a KV_OK / KV_ERR_* code (static string). */
+const char* kv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATHER_TRANSLATE_KV_GB300_KV_POOL_H */

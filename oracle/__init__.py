@@ -108,6 +108,12 @@ def lib(path: str | None = None):
         L.ora_gather.restype = ctypes.c_int
         L.ora_move.argtypes = [P(_Desc), vp, vp, vp, c64]
         L.ora_move.restype = ctypes.c_int
+        L.ora_store_rows.argtypes = [P(_Desc), c32, vp, c64, vp, c64, vp, vp]
+        L.ora_store_rows.restype = ctypes.c_int
+        L.ora_gather_rows.argtypes = [P(_Desc), c32, vp, c32, c32, vp, vp, vp, c64, vp, vp]
+        L.ora_gather_rows.restype = ctypes.c_int
+        L.ora_move_rows.argtypes = [P(_Desc), vp, vp, c64, vp, vp]
+        L.ora_move_rows.restype = ctypes.c_int
         if path is not None:
             return L
         _lib = L
@@ -219,3 +225,39 @@ class Oracle:
         d = np.ascontiguousarray(dst_ids, dtype=np.int32)
         assert s.size == d.size
         return self._L.ora_move(ctypes.byref(self._d), _ptr(M), _ptr(s), _ptr(d), s.size)
+
+    # address mode ----------------------------------------------------------
+    def store_rows(self, layer: int, slots, v2p=None):
+        """Byte offsets a store of ``slots`` writes: (kdst[n], vdst[n], err)."""
+        slots = np.ascontiguousarray(slots, dtype=np.int64)
+        kd = np.empty(slots.size, np.int64)
+        vd = np.empty(slots.size, np.int64)
+        v = None if v2p is None else np.ascontiguousarray(v2p, dtype=np.int32)
+        err = self._L.ora_store_rows(ctypes.byref(self._d), int(layer), _ptr(slots), slots.size,
+                                     _ptr(v), 0 if v is None else v.size, _ptr(kd), _ptr(vd))
+        return kd, vd, err
+
+    def gather_rows(self, layer, block_table, seq_len, cu, seq_start=None, out_rows=None):
+        """Byte offsets each output row reads: (ksrc[out_rows], vsrc[out_rows], err), -1 = untouched."""
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        n_seqs, max_pages = bt.shape
+        ln = np.ascontiguousarray(seq_len, dtype=np.int32)
+        cu = np.ascontiguousarray(cu, dtype=np.int64)
+        st = None if seq_start is None else np.ascontiguousarray(seq_start, dtype=np.int32)
+        if out_rows is None:
+            out_rows = int(cu[-1]) if n_seqs > 0 else 0
+        ks = np.full(out_rows, -1, np.int64)
+        vs = np.full(out_rows, -1, np.int64)
+        err = self._L.ora_gather_rows(ctypes.byref(self._d), int(layer), _ptr(bt), n_seqs, max_pages,
+                                      _ptr(st), _ptr(ln), _ptr(cu), out_rows, _ptr(ks), _ptr(vs))
+        return ks, vs, err
+
+    def move_rows(self, src_ids, dst_ids):
+        """Byte offsets a move reads and writes: (src[m*2L], dst[m*2L], err)."""
+        s = np.ascontiguousarray(src_ids, dtype=np.int32)
+        d = np.ascontiguousarray(dst_ids, dtype=np.int32)
+        nb = 2 * self.geom.layer_num
+        sb = np.empty(s.size * nb, np.int64)
+        db = np.empty(s.size * nb, np.int64)
+        err = self._L.ora_move_rows(ctypes.byref(self._d), _ptr(s), _ptr(d), s.size, _ptr(sb), _ptr(db))
+        return sb, db, err

@@ -213,10 +213,14 @@ int64_t ora_slot_row_byte(const ora_desc* d, int64_t slot, const int32_t* v2p,
  * goes to block 2l and its V to block 2l+1 of the page that slot i lives on
  * (实现拆解 step 1). K and V are [n, H, D] contiguous, R bytes per row.
  * Rows are written in input order; several tombstones all land on the sink
- * rows (page 0, offset 0), the last one written stays. */
-int ora_store(const ora_desc* d, uint8_t* M, int32_t layer, const int64_t* slots,
-              int64_t n, const int32_t* v2p, int64_t v2p_len,
-              const uint8_t* K, const uint8_t* V) {
+ * rows (page 0, offset 0), the last one written stays.
+ *
+ * With M == NULL nothing is copied: the pass records, for every row i, the
+ * byte offsets it would write (kdst[i], vdst[i]); tests use this to check a
+ * full-size run without a host mirror of the pool. */
+static int store_pass(const ora_desc* d, uint8_t* M, int32_t layer, const int64_t* slots,
+                      int64_t n, const int32_t* v2p, int64_t v2p_len,
+                      const uint8_t* K, const uint8_t* V, int64_t* kdst, int64_t* vdst) {
     int64_t s[7];
     ora_sizes(d, s);
     int64_t R = s[0];
@@ -226,10 +230,29 @@ int ora_store(const ora_desc* d, uint8_t* M, int32_t layer, const int64_t* slots
         int64_t p, o;
         int sink;
         err |= locate_slot(d, slots[i], v2p, v2p_len, &p, &o, &sink);
-        memcpy(M + env_byte(d, p, 2 * (int64_t)layer, o), K + i * R, (size_t)R);
-        memcpy(M + env_byte(d, p, 2 * (int64_t)layer + 1, o), V + i * R, (size_t)R);
+        int64_t kb = env_byte(d, p, 2 * (int64_t)layer, o);
+        int64_t vb = env_byte(d, p, 2 * (int64_t)layer + 1, o);
+        if (M != NULL) {
+            memcpy(M + kb, K + i * R, (size_t)R);
+            memcpy(M + vb, V + i * R, (size_t)R);
+        } else {
+            kdst[i] = kb;
+            vdst[i] = vb;
+        }
     }
     return err;
+}
+
+int ora_store(const ora_desc* d, uint8_t* M, int32_t layer, const int64_t* slots,
+              int64_t n, const int32_t* v2p, int64_t v2p_len,
+              const uint8_t* K, const uint8_t* V) {
+    if (M == NULL) return -1;
+    return store_pass(d, M, layer, slots, n, v2p, v2p_len, K, V, NULL, NULL);
+}
+
+int ora_store_rows(const ora_desc* d, int32_t layer, const int64_t* slots, int64_t n,
+                   const int32_t* v2p, int64_t v2p_len, int64_t* kdst, int64_t* vdst) {
+    return store_pass(d, NULL, layer, slots, n, v2p, v2p_len, NULL, NULL, kdst, vdst);
 }
 
 /* All-layer store: ora_store for l = 0..L-1 with K_all[l], V_all[l]; the
@@ -263,10 +286,11 @@ int ora_store_all(const ora_desc* d, uint8_t* M, const int64_t* slots, int64_t n
  * j is negative, or whose output row falls outside [0, out_rows) is skipped.
  * A page >= P raises ORA_E_ROW and the token is skipped. Skipped tokens leave
  * their output rows untouched. */
-int ora_gather(const ora_desc* d, const uint8_t* M, int32_t layer,
-               const int32_t* bt, int32_t n_seqs, int32_t max_pages,
-               const int32_t* seq_start, const int32_t* seq_len,
-               const int64_t* cu, uint8_t* outK, uint8_t* outV, int64_t out_rows) {
+static int gather_pass(const ora_desc* d, const uint8_t* M, int32_t layer,
+                       const int32_t* bt, int32_t n_seqs, int32_t max_pages,
+                       const int32_t* seq_start, const int32_t* seq_len,
+                       const int64_t* cu, uint8_t* outK, uint8_t* outV, int64_t out_rows,
+                       int64_t* ksrc, int64_t* vsrc) {
     int64_t s7[7];
     ora_sizes(d, s7);
     int64_t R = s7[0];
@@ -290,11 +314,36 @@ int ora_gather(const ora_desc* d, const uint8_t* M, int32_t layer,
             if (p >= d->num_pages) { err |= ORA_E_ROW; continue; }
             int64_t r = cu[s] + (j - st);
             if (r < 0 || r >= out_rows) continue;
-            memcpy(outK + r * R, M + env_byte(d, p, 2 * (int64_t)layer, o), (size_t)R);
-            memcpy(outV + r * R, M + env_byte(d, p, 2 * (int64_t)layer + 1, o), (size_t)R);
+            int64_t kb = env_byte(d, p, 2 * (int64_t)layer, o);
+            int64_t vb = env_byte(d, p, 2 * (int64_t)layer + 1, o);
+            if (M != NULL) {
+                memcpy(outK + r * R, M + kb, (size_t)R);
+                memcpy(outV + r * R, M + vb, (size_t)R);
+            } else {
+                ksrc[r] = kb;
+                vsrc[r] = vb;
+            }
         }
     }
     return err;
+}
+
+int ora_gather(const ora_desc* d, const uint8_t* M, int32_t layer,
+               const int32_t* bt, int32_t n_seqs, int32_t max_pages,
+               const int32_t* seq_start, const int32_t* seq_len,
+               const int64_t* cu, uint8_t* outK, uint8_t* outV, int64_t out_rows) {
+    if (M == NULL) return -1;
+    return gather_pass(d, M, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu,
+                       outK, outV, out_rows, NULL, NULL);
+}
+
+/* Address mode of ora_gather: ksrc[r] / vsrc[r] receive the pool byte offset
+ * output row r reads (rows no token covers are left as the caller set them). */
+int ora_gather_rows(const ora_desc* d, int32_t layer, const int32_t* bt, int32_t n_seqs,
+                    int32_t max_pages, const int32_t* seq_start, const int32_t* seq_len,
+                    const int64_t* cu, int64_t out_rows, int64_t* ksrc, int64_t* vsrc) {
+    return gather_pass(d, NULL, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu,
+                       NULL, NULL, out_rows, ksrc, vsrc);
 }
 
 /* ------------------------------------------------------------------- move */
@@ -354,4 +403,23 @@ int64_t ora_id_row_byte(const ora_desc* d, int64_t id, int32_t block) {
     int64_t p, o;
     if (decode_id(d, id, &p, &o) != 0) return -1;
     return env_byte(d, p, block, o);
+}
+
+/* Address mode of ora_move: for pair i and block b, src_bytes[i*2L + b] and
+ * dst_bytes[i*2L + b] receive the byte offsets the move reads and writes, or
+ * -1 for a skipped pair. Returns the same error bits as ora_move. */
+int ora_move_rows(const ora_desc* d, const int32_t* src_ids, const int32_t* dst_ids,
+                  int64_t m, int64_t* src_bytes, int64_t* dst_bytes) {
+    int64_t blocks = 2 * (int64_t)d->layer_num;
+    int err = 0;
+    for (int64_t i = 0; i < m; ++i) {
+        int64_t ps_ = 0, os_ = 0, pd_ = 0, od_ = 0;
+        int e = decode_id(d, src_ids[i], &ps_, &os_) | decode_id(d, dst_ids[i], &pd_, &od_);
+        err |= e;
+        for (int64_t b = 0; b < blocks; ++b) {
+            src_bytes[i * blocks + b] = e ? -1 : env_byte(d, ps_, b, os_);
+            dst_bytes[i * blocks + b] = e ? -1 : env_byte(d, pd_, b, od_);
+        }
+    }
+    return err;
 }

@@ -345,3 +345,28 @@ def move_slots(shape: Shape, m: int | None = None, avoid: np.ndarray | None = No
         return src.astype(np.int64), dst.astype(np.int64)
     both = distinct_slots(rng, ps, P * ps, 2 * m)
     return both[:m].copy(), both[m:].copy()
+
+
+def sentinel_rows_torch(fill_seed: int, byte_offsets, row_bytes: int, chunk_rows: int = 1 << 16):
+    """Sentinel content of many rows, computed on the offsets' device:
+    uint8 [n, row_bytes]. Offsets and row_bytes must be multiples of 8."""
+    import torch
+
+    assert row_bytes % 8 == 0
+    offs = byte_offsets.to(torch.int64)
+    n = offs.numel()
+    out = torch.empty((n, row_bytes), dtype=torch.uint8, device=offs.device)
+    words_out = out.view(torch.int64).view(n, row_bytes // 8)
+    inc, m1, m2 = _i64(0x9E3779B97F4A7C15), _i64(0xBF58476D1CE4E5B9), _i64(0x94D049BB133111EB)
+    mask = {k: (1 << (64 - k)) - 1 for k in (30, 27, 31)}
+    lane = torch.arange(row_bytes // 8, dtype=torch.int64, device=offs.device)
+    for r0 in range(0, n, chunk_rows):
+        r1 = min(n, r0 + chunk_rows)
+        z = (offs[r0:r1, None] // 8) + lane[None, :]
+        z.bitwise_xor_(int(fill_seed))
+        z.add_(inc)
+        z.bitwise_xor_(torch.bitwise_right_shift(z, 30).bitwise_and_(mask[30])).mul_(m1)
+        z.bitwise_xor_(torch.bitwise_right_shift(z, 27).bitwise_and_(mask[27])).mul_(m2)
+        z.bitwise_xor_(torch.bitwise_right_shift(z, 31).bitwise_and_(mask[31]))
+        words_out[r0:r1].copy_(z)
+    return out

@@ -315,9 +315,45 @@ def pin_errors(so):
     assert err == oracle.E_TABLE
 
 
+def pin_address_mode(so):
+    """The address-mode routines (used to check full-size runs) name exactly
+    the bytes the copying routines move."""
+    rng = np.random.default_rng(16)
+    L, H, D, it, ps, P = 3, 1, 16, 2, 4, 12
+    o = _mk(so, _geom(L, H, D, it, ps, P))
+    R = o.sizes()["row_bytes"]
+    slots = rng.permutation(np.arange(ps, P * ps))[:20].astype(np.int64)
+    K = synth.kv_values(rng, (20, H, D), it)
+    V = synth.kv_values(rng, (20, H, D), it)
+    M = _fresh(o)
+    T = M.copy()
+    assert o.store(M, 2, slots, K, V) == 0
+    kd, vd, err = o.store_rows(2, slots)
+    assert err == 0
+    Kb, Vb = K.reshape(20, -1).view(np.uint8), V.reshape(20, -1).view(np.uint8)
+    for i in range(20):
+        T[kd[i]:kd[i] + R] = Kb[i]
+        T[vd[i]:vd[i] + R] = Vb[i]
+    assert np.array_equal(M, T)
+    bt = rng.integers(1, P, size=(3, 4)).astype(np.int32)
+    g = synth.GatherBatch(bt, np.array([0, 2, 5], np.int32), np.array([16, 9, 5], np.int32))
+    k, v, err = o.gather(M, 1, bt, g.seq_len, g.cu, g.seq_start)
+    ks, vs, err2 = o.gather_rows(1, bt, g.seq_len, g.cu, g.seq_start)
+    assert err == err2 == 0
+    for r in range(g.total):
+        assert np.array_equal(k[r], M[ks[r]:ks[r] + R]) and np.array_equal(v[r], M[vs[r]:vs[r] + R])
+    src, _ = o.translate(slots[:5])
+    dst, _ = o.translate(np.setdiff1d(np.arange(ps, P * ps), slots)[:5])
+    sb, db, err = o.move_rows(src, dst)
+    before = M.copy()
+    assert err == 0 and o.move(M, src, dst) == 0
+    for a, b in zip(sb, db):
+        assert np.array_equal(M[b:b + R], before[a:a + R])
+
+
 PINS = [
     pin_translate_golden, pin_layout_table, pin_gates, pin_bijection, pin_store_vs_strided,
-    pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors,
+    pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors, pin_address_mode,
 ]
 
 

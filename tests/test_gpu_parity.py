@@ -1,0 +1,327 @@
+"""GPU parity: every entry point through the C ABI against the CPU oracle,
+byte for byte, on pools small enough to mirror whole on the host.
+
+The shapes keep the model geometry of each workload (rows of 32 B to 4 KiB,
+page sizes 3 to 256, fp8 and bf16) on fewer pages, with token counts that
+span several warps' tiles and end in a ragged tail. Inputs are seeded.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import gather_translate_kv_gb300 as gt
+import oracle
+import synth
+from gpu_util import PoolPair, as_rows, assert_bytes_equal, assert_pool_matches, dev_bits, merge, to_dev, \
+    tomb_inputs
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gather_translate_kv_gb300 import build
+
+    build.build()
+    oracle.build()
+
+
+S = synth.Shape
+SHAPES = [
+    (synth.SHAPES[1], 0),                       # R=32, ps=4 (general row path)
+    (synth.SHAPES[2].scaled(40), 0),            # R=2048, ps=16, L=32
+    (synth.SHAPES[3].scaled(12), 64),           # R=2048, ps=64, anchor 64
+    (synth.SHAPES[4].scaled(150), 0),           # R=512 fp8, ps=32, L=24
+    (synth.SHAPES[5].scaled(20), 0),            # R=64 fp8, ps=256, L=80
+    (S(0, "odd-rows", 3, 3, 16, 1, 3, 40), 16),  # R=48 (general path), ps=3
+    (S(0, "wide-rows", 2, 12, 128, 1, 5, 24), 0),  # R=1536 (general path), ps=5
+    (S(0, "r4096", 2, 16, 128, 2, 8, 12), 32),  # R=4096
+    (S(0, "r256", 4, 2, 64, 2, 4, 30), 0),      # R=256
+    (S(0, "r128", 4, 1, 64, 2, 2, 40), 0),      # R=128
+    (S(0, "r1024", 2, 4, 128, 2, 16, 10), 0),   # R=1024
+    (S(0, "fp32-r1024", 2, 2, 128, 4, 12, 10), 0),  # R=1024, ps=12
+]
+IDS = [f"{s.name}-R{s.row_bytes}-ps{s.page_size}" for s, _ in SHAPES]
+
+
+def _tokens(shape: synth.Shape, rng, n: int, tomb: int) -> np.ndarray:
+    ps, P = shape.page_size, shape.num_pages
+    n = min(n, (P - 1) * ps)
+    slots = synth.distinct_slots(rng, ps, P * ps, n)
+    return synth.with_tombstones(rng, slots, min(tomb, n))
+
+
+def _vals(shape, rng, lead):
+    dims = tuple(lead) + (shape.head_num, shape.head_dim)
+    return synth.kv_values(rng, dims, shape.itemsize), synth.kv_values(rng, dims, shape.itemsize)
+
+
+def test_translate_golden():
+    pp = PoolPair(synth.SHAPES[1])
+    maps = {
+        "none": None,
+        "tomb1": np.where(np.arange(64) == 1, -1, np.arange(64)).astype(np.int32),
+        "p1to9": np.where(np.arange(64) == 1, 9, np.arange(64)).astype(np.int32),
+    }
+    for line in open(os.path.join(GOLDEN, "translate_tiny.txt")):
+        line = line.split("#", 1)[0].split()
+        if not line:
+            continue
+        slot, case, want = int(line[0]), line[1], int(line[2])
+        ids = torch.empty(1, dtype=torch.int32, device="cuda")
+        v2p = None if maps[case] is None else to_dev(maps[case])
+        gt.kv_translate(pp.pool, to_dev(np.array([slot], np.int64)), ids, v2p)
+        assert int(ids.item()) == want, (slot, case)
+    assert pp.last_error() == 0
+
+
+@pytest.mark.parametrize("shape,anchor", SHAPES, ids=IDS)
+def test_translate_matches_oracle(shape, anchor):
+    rng = np.random.default_rng(100 + shape.row_bytes + shape.page_size)
+    pp = PoolPair(shape, anchor, mirror=False)
+    ps, P = shape.page_size, shape.num_pages
+    n = 5000
+    slots = rng.integers(-3, P * ps, size=n).astype(np.int64)
+    # without a page map
+    ids_ref, err = pp.o.translate(slots)
+    ids = torch.empty(n, dtype=torch.int32, device="cuda")
+    gt.kv_translate(pp.pool, to_dev(slots), ids)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert pp.last_error() == dev_bits(err) == 0
+    # with a page map: a permutation with tombstoned pages
+    v2p = rng.permutation(P).astype(np.int32)
+    v2p[rng.choice(P, size=max(1, P // 7), replace=False)] = -1
+    ids_ref, err = pp.o.translate(slots, v2p)
+    gt.kv_translate(pp.pool, to_dev(slots), ids, to_dev(v2p))
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert pp.last_error() == dev_bits(err) == 0
+    # errors: a map shorter than the slots' pages, and pages past the pool
+    short = v2p[: P // 2].copy()
+    short[0] = P + 3
+    ids_ref, err = pp.o.translate(slots, short)
+    gt.kv_translate(pp.pool, to_dev(slots), ids, to_dev(short))
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert err == oracle.E_V2P | oracle.E_ROW
+    assert pp.last_error() == dev_bits(err)
+    pp.close()
+
+
+@pytest.mark.parametrize("shape,anchor", SHAPES, ids=IDS)
+def test_path_matches_oracle(shape, anchor):
+    """translate -> per-layer stores -> all-layer store -> gathers -> move,
+    comparing the whole pool (and every output) after each step."""
+    rng = np.random.default_rng(200 + shape.row_bytes * 7 + shape.page_size)
+    pp = PoolPair(shape, anchor)
+    o, R, L = pp.o, pp.R, shape.layer_num
+    ps, P = shape.page_size, shape.num_pages
+    M0 = pp.M.copy()
+    tombs: dict = {}
+    stored = set()
+
+    # per-layer stores through translate (K1 -> K2)
+    for layer in sorted({0, L // 2, L - 1}):
+        n = 37 * 11 if shape.cfg != 1 else 100
+        slots = synth.store_slots(shape, layer) if shape.cfg == 1 else _tokens(shape, rng, n, 9)
+        K, V = _vals(shape, rng, (slots.size,))
+        err = o.store(pp.M, layer, slots, K, V)
+        ids_ref, terr = o.translate(slots)
+        ids = torch.empty(slots.size, dtype=torch.int32, device="cuda")
+        gt.kv_translate(pp.pool, to_dev(slots), ids)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        gt.kv_store_layer(pp.pool, layer, ids, to_dev(K), to_dev(V))
+        assert pp.last_error() == dev_bits(err | terr) == 0
+        tombs = merge(tombs, tomb_inputs(slots, K, V, layer, R))
+        stored.update(int(t) for t in slots if t >= 0)
+        assert_pool_matches(pp, M0, tombs)
+
+    # all-layer store
+    n = 300 if shape.cfg != 1 else 100
+    slots = _tokens(shape, rng, n, 4)
+    Ka, Va = _vals(shape, rng, (L, slots.size))
+    err = o.store_all(pp.M, slots, Ka, Va)
+    ids = torch.empty(slots.size, dtype=torch.int32, device="cuda")
+    gt.kv_translate(pp.pool, to_dev(slots), ids)
+    gt.kv_store_all_layers(pp.pool, ids, to_dev(Ka), to_dev(Va))
+    assert pp.last_error() == dev_bits(err) == 0
+    for layer in range(L):
+        tombs = merge(tombs, tomb_inputs(slots, Ka[layer], Va[layer], layer, R))
+    stored.update(int(t) for t in slots if t >= 0)
+    assert_pool_matches(pp, M0, tombs)
+
+    # gathers: full sequences, windows starting mid-page, an empty sequence,
+    # ragged lengths, pages shared across sequences (never page 0)
+    if shape.cfg == 1:
+        g = synth.gather_batch(shape)
+        batches = [g, synth.GatherBatch(g.block_table, np.array([3], np.int32), np.array([29], np.int32))]
+    else:
+        S_, maxp = 9, min(P - 1, 7)
+        bt = np.stack([1 + rng.permutation(P - 1)[:maxp] for _ in range(S_)]).astype(np.int32)
+        ln = rng.integers(0, maxp * ps + 1, size=S_).astype(np.int32)
+        ln[2] = 0
+        ln[0] = maxp * ps
+        st = np.minimum(rng.integers(0, 2 * ps, size=S_), ln).astype(np.int32)
+        batches = [synth.GatherBatch(bt, np.zeros(S_, np.int32), ln), synth.GatherBatch(bt, st, ln)]
+    for gb in batches:
+        for layer in sorted({0, L - 1}):
+            rows = gb.total + 5  # a few spare rows must stay untouched
+            ok = np.full((rows, R), 0x5A, np.uint8)
+            ov = np.full((rows, R), 0xA5, np.uint8)
+            ok, ov, err = o.gather(pp.M, layer, gb.block_table, gb.seq_len, gb.cu, gb.seq_start, rows, ok, ov)
+            dk = torch.full((rows, R), 0x5A, dtype=torch.uint8, device="cuda")
+            dv = torch.full((rows, R), 0xA5, dtype=torch.uint8, device="cuda")
+            gt.kv_gather_layer(pp.pool, layer, to_dev(gb.block_table), to_dev(gb.seq_len), to_dev(gb.cu), dk, dv,
+                               to_dev(gb.seq_start))
+            assert pp.last_error() == dev_bits(err) == 0
+            assert_bytes_equal(dk.cpu().numpy(), ok, f"gather K layer {layer}", R)
+            assert_bytes_equal(dv.cpu().numpy(), ov, f"gather V layer {layer}", R)
+
+    # move: stored tokens -> never-stored tokens (disjoint, distinct)
+    if shape.cfg == 1:
+        src_slots = rng.choice(sorted(stored), size=20, replace=False).astype(np.int64)
+    else:
+        src_slots = rng.choice(sorted(stored), size=min(len(stored), 150), replace=False).astype(np.int64)
+    free = np.setdiff1d(np.arange(ps, P * ps, dtype=np.int64), np.array(sorted(stored), np.int64))
+    dst_slots = rng.choice(free, size=src_slots.size, replace=False).astype(np.int64)
+    src_ids, _ = o.translate(src_slots)
+    dst_ids, _ = o.translate(dst_slots)
+    err = o.move(pp.M, src_ids, dst_ids)
+    gt.kv_move(pp.pool, to_dev(src_ids), to_dev(dst_ids))
+    assert pp.last_error() == dev_bits(err) == 0
+    assert_pool_matches(pp, M0, tombs)
+    pp.close()
+
+
+def test_error_paths_match_oracle():
+    shape = S(0, "err", 2, 1, 64, 2, 4, 16)  # R=128
+    rng = np.random.default_rng(7)
+    pp = PoolPair(shape)
+    o, R, ps, P = pp.o, pp.R, shape.page_size, shape.num_pages
+    M0 = pp.M.copy()
+    n_rows = pp.sizes["n_rows"]
+    # store: ids outside [0, n_rows) are skipped and flagged
+    slots = synth.distinct_slots(rng, ps, P * ps, 40)
+    K, V = _vals(shape, rng, (40,))
+    ids, _ = o.translate(slots)
+    bad = ids.copy()
+    bad[[3, 17, 39]] = [n_rows, -5, n_rows + 1000]
+    keep = np.ones(40, bool)
+    keep[[3, 17, 39]] = False
+    o.store(pp.M, 1, slots[keep], K[keep], V[keep])
+    gt.kv_store_layer(pp.pool, 1, to_dev(bad), to_dev(K), to_dev(V))
+    assert pp.last_error() == gt.KV_DEV_ERR_ROW
+    assert_pool_matches(pp, M0, {})
+    # move: a non-translate-form id and an out-of-range id skip their pairs
+    src, _ = o.translate(slots[:6])
+    free = np.setdiff1d(np.arange(ps, P * ps), slots)[:6]
+    dst, _ = o.translate(free)
+    src_b = src.copy()
+    dst_b = dst.copy()
+    src_b[1] = src[1] + ps  # offset >= ps inside its page envelope
+    dst_b[4] = n_rows + 7
+    err = o.move(pp.M, src_b, dst_b)
+    assert err == oracle.E_FORM | oracle.E_ROW
+    gt.kv_move(pp.pool, to_dev(src_b), to_dev(dst_b))
+    assert pp.last_error() == dev_bits(err)
+    assert_pool_matches(pp, M0, {})
+    # gather: a page past the pool, a sequence whose cu span is too short, and
+    # an output too small for cu[S]
+    bt = np.array([[1, 2, P + 4, 3], [4, 5, 6, 7], [8, 9, 10, 11]], np.int32)
+    ln = np.array([16, 16, 10], np.int32)
+    st = np.array([0, 2, 1], np.int32)
+    cu = np.array([0, 16, 27, 40], np.int64)  # sequence 1 needs 14 rows, gets 11
+    for rows in (40, 33):
+        ok = np.full((rows, R), 1, np.uint8)
+        ov = np.full((rows, R), 2, np.uint8)
+        ok, ov, err = o.gather(pp.M, 0, bt, ln, cu, st, rows, ok, ov)
+        dk = torch.full((rows, R), 1, dtype=torch.uint8, device="cuda")
+        dv = torch.full((rows, R), 2, dtype=torch.uint8, device="cuda")
+        gt.kv_gather_layer(pp.pool, 0, to_dev(bt), to_dev(ln), to_dev(cu), dk, dv, to_dev(st))
+        assert err == oracle.E_ROW | oracle.E_TABLE
+        assert pp.last_error() == dev_bits(err)
+        # rows the oracle writes and the kernel writes agree wherever the
+        # metadata is consistent (sequences 0 and 2)
+        for r0, r1 in ((0, 16), (27, min(rows, 36))):
+            assert_bytes_equal(dk.cpu().numpy()[r0:r1], ok[r0:r1], "gather K", R)
+            assert_bytes_equal(dv.cpu().numpy()[r0:r1], ov[r0:r1], "gather V", R)
+    # host-side argument errors
+    with pytest.raises(gt.KVError) as e:
+        gt.kv_store_layer(pp.pool, 2, to_dev(ids), to_dev(K), to_dev(V))
+    assert e.value.name == "KV_ERR_INVALID"
+    with pytest.raises(gt.KVError) as e:
+        kk = torch.empty(40 * R + 8, dtype=torch.uint8, device="cuda")[8:]
+        gt.kv_store_layer(pp.pool, 0, to_dev(ids), kk, to_dev(V))
+    assert e.value.name == "KV_ERR_ALIGN"
+    pp.close()
+
+
+def test_gather_tombstoned_table_entry_reads_sink():
+    shape = S(0, "sink", 2, 2, 64, 2, 8, 10)
+    pp = PoolPair(shape)
+    bt = np.array([[3, -1, 5]], np.int32)
+    g = synth.GatherBatch(bt, np.array([4], np.int32), np.array([22], np.int32))
+    ok, ov, err = pp.o.gather(pp.M, 1, bt, g.seq_len, g.cu, g.seq_start)
+    dk = torch.zeros((g.total, pp.R), dtype=torch.uint8, device="cuda")
+    dv = torch.zeros_like(dk)
+    gt.kv_gather_layer(pp.pool, 1, to_dev(bt), to_dev(g.seq_len), to_dev(g.cu), dk, dv, to_dev(g.seq_start))
+    assert err == 0 and pp.last_error() == 0
+    assert_bytes_equal(dk.cpu().numpy(), ok, "K", pp.R)
+    assert_bytes_equal(dv.cpu().numpy(), ov, "V", pp.R)
+    sink_k = pp.M[pp.o.slot_row_byte(0, 2): pp.o.slot_row_byte(0, 2) + pp.R]
+    assert np.array_equal(ok[8 - 4], sink_k)  # token 8 sits on the tombstoned page
+
+
+def test_calls_capture_in_a_cuda_graph():
+    """translate -> store -> gather captured once, replayed on new inputs."""
+    shape = synth.SHAPES[2].scaled(24)
+    pp = PoolPair(shape)
+    o, R, ps, P = pp.o, pp.R, shape.page_size, shape.num_pages
+    M0 = pp.M.copy()
+    n = 64
+    slots_d = torch.zeros(n, dtype=torch.int64, device="cuda")
+    ids_d = torch.zeros(n, dtype=torch.int32, device="cuda")
+    k_d = torch.zeros((n, R), dtype=torch.uint8, device="cuda")
+    v_d = torch.zeros_like(k_d)
+    bt = np.stack([1 + np.arange(8) + 8 * s for s in range(2)]).astype(np.int32)
+    g = synth.GatherBatch(bt, np.zeros(2, np.int32), np.full(2, 8 * ps, np.int32))
+    bt_d, ln_d, cu_d = to_dev(bt), to_dev(g.seq_len), to_dev(g.cu)
+    ok_d = torch.zeros((g.total, R), dtype=torch.uint8, device="cuda")
+    ov_d = torch.zeros_like(ok_d)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture
+        gt.kv_translate(pp.pool, slots_d, ids_d)
+        gt.kv_store_layer(pp.pool, 3, ids_d, k_d, v_d)
+        gt.kv_gather_layer(pp.pool, 3, bt_d, ln_d, cu_d, ok_d, ov_d)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    # restore the pool and the mirror to the sentinel before the replays
+    synth.fill_sentinel_torch(pp.raw, pp.fill_seed)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gt.kv_translate(pp.pool, slots_d, ids_d)
+        gt.kv_store_layer(pp.pool, 3, ids_d, k_d, v_d)
+        gt.kv_gather_layer(pp.pool, 3, bt_d, ln_d, cu_d, ok_d, ov_d)
+    rng = np.random.default_rng(9)
+    for rep in range(2):
+        slots = synth.distinct_slots(rng, ps, 17 * ps, n)  # pages the gather reads
+        K, V = _vals(shape, rng, (n,))
+        slots_d.copy_(to_dev(slots))
+        k_d.copy_(to_dev(as_rows(K, R)))
+        v_d.copy_(to_dev(as_rows(V, R)))
+        o.store(pp.M, 3, slots, K, V)
+        graph.replay()
+        torch.cuda.synchronize()
+        rk, rv, _ = o.gather(pp.M, 3, bt, g.seq_len, g.cu)
+        assert_bytes_equal(ok_d.cpu().numpy(), rk, "graph gather K", R)
+        assert_bytes_equal(ov_d.cpu().numpy(), rv, "graph gather V", R)
+        assert_pool_matches(pp, M0, {})
+    assert pp.last_error() == 0
+    pp.close()

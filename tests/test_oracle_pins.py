@@ -34,11 +34,11 @@ MUTANTS = [
      "b * ((int64_t)d->page_size * R) + o * R;",
      "o * ((int64_t)d->page_size * R) + b * R;"),
     ("v_written_to_k_block",
-     "memcpy(M + env_byte(d, p, 2 * (int64_t)layer + 1, o), V + i * R, (size_t)R);",
-     "memcpy(M + env_byte(d, p, 2 * (int64_t)layer, o), V + i * R, (size_t)R);"),
+     "memcpy(M + vb, V + i * R, (size_t)R);",
+     "memcpy(M + kb, V + i * R, (size_t)R);"),
     ("k_and_v_blocks_swapped_in_gather",
-     "memcpy(outK + r * R, M + env_byte(d, p, 2 * (int64_t)layer, o), (size_t)R);",
-     "memcpy(outK + r * R, M + env_byte(d, p, 2 * (int64_t)layer + 1, o), (size_t)R);"),
+     "memcpy(outK + r * R, M + kb, (size_t)R);",
+     "memcpy(outK + r * R, M + vb, (size_t)R);"),
     ("gather_output_row_ignores_start",
      "int64_t r = cu[s] + (j - st);",
      "int64_t r = cu[s] + j;"),
