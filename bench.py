@@ -223,6 +223,26 @@ def oracle_sample(budget_s: float = 12.0):
             "seconds": el}
 
 
+# ------------------------------------------------------------------ ranks
+
+def reduce_max(values, device=None):
+    """Max over ranks of per-rank timings (identity when not distributed).
+    Every rank gets the result; rank 0 prints it."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_gbps(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank moves its own step's bytes; the job's rate is
+    all ranks' bytes over the slowest rank's time."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / GB
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_gpu(args):
@@ -347,10 +367,7 @@ def run_gpu(args):
 
     ub = useful_bytes()
     step_bytes = sum(ub.values())
-    ms_t = torch.tensor([ms, e2e_s * 1e3, gather_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms, e2e_ms, gather_ms = ms_t.tolist()
+    ms, e2e_ms, gather_ms = reduce_max([ms, e2e_s * 1e3, gather_ms], dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -361,7 +378,7 @@ def run_gpu(args):
     traffic = profiled_traffic(os.path.join(ROOT, "gather_translate_kv_gb300", "csrc", "kv_gather.cu"))
     line = {
         "metric": "KV store/gather/move useful GB/s and % of GB300 HBM peak (byte-exact vs oracle)",
-        "value": round(step_bytes * world / (ms * 1e-3) / GB, 1),
+        "value": round(whole_job_gbps(step_bytes, world, ms), 1),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -380,7 +397,7 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": gather_bytes, "avg_launch_ms": round(gather_ms, 4)},
-        "e2e": {"value": round(step_bytes * world / (e2e_ms * 1e-3) / GB, 1), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbps(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -423,6 +440,185 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ per-kernel table
+
+MICRO_DEFAULT = ["translate:2", "store:2", "store_graph:2", "store_all:2", "gather:2", "move:2",
+                 "translate:3", "store:3", "store_all:3", "gather:3",
+                 "store:4", "gather:4", "move:4",
+                 "translate:5", "store:5", "gather:5", "move:5"]
+
+
+def _payload_torch(gen, rows: int, R: int, itemsize: int, dev):
+    """Seeded synthetic K or V rows on the device: bf16 N(0,1) bits, or fp8
+    e4m3 bytes uniform over the 254 non-NaN codes."""
+    import torch
+
+    if itemsize == 2:
+        return torch.randn((rows, R // 2), generator=gen, device=dev, dtype=torch.float32) \
+            .to(torch.bfloat16).view(torch.uint8).reshape(rows, R)
+    x = torch.randint(0, 254, (rows, R), generator=gen, device=dev, dtype=torch.int16)
+    x += (x >= 0x7F).to(torch.int16)
+    return x.to(torch.uint8)
+
+
+def run_micro(args):
+    """Each kernel on each workload of the build plan, timed per launch with
+    CUDA events (median), L2 flushed between launches whose working set is
+    under 4x the L2 size (a 2x-L2 write followed by a 2x-L2 read, so the
+    launch finds neither its data nor dirty lines in L2). One JSON line per
+    (kernel, workload)."""
+    import torch
+
+    import gather_translate_kv_gb300 as gt
+    from gather_translate_kv_gb300 import build as gbuild
+
+    gbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = measured_hbm_peak()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_read = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one: the timed
+        # launch starts with none of its data cached and no dirty lines left
+        # for it to write back
+        flush_buf.zero_()
+        flush_read.max()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    stream = torch.cuda.current_stream(dev)
+    todo = args.only.split(",") if args.only else MICRO_DEFAULT
+    by_cfg: dict[int, list[str]] = {}
+    for item in todo:
+        k, c = item.split(":")
+        by_cfg.setdefault(int(c), []).append(k)
+
+    def timed(fn, calls: int, flush: bool):
+        ms = []
+        for i in range(calls + 3):
+            if flush:
+                flush_l2()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(i)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                ms.append(e0.elapsed_time(e1))
+        return ms
+
+    def report(kernel, cfg, workload, ms, useful, rows, extra=None):
+        med = statistics.median(ms)
+        line = {"micro": kernel, "cfg": cfg, "workload": workload, "calls": len(ms),
+                "us_per_call": round(med * 1e3, 2), "useful_bytes_per_call": useful,
+                "useful_GBps": round(useful / (med * 1e-3) / GB, 1),
+                "pct_of_hbm_peak": round(100 * useful / (med * 1e-3) / GB / peak, 1),
+                "rows_per_s": round(rows / (med * 1e-3), 1), "peak_GBps": peak, "peak_source": peak_kind}
+        line.update(extra or {})
+        print(json.dumps(line), flush=True)
+
+    for cfg, kernels in sorted(by_cfg.items()):
+        sh = synth.SHAPES[cfg]
+        if args.pages or args.layers:
+            sh = synth.Shape(cfg, sh.name + "-small", args.layers or sh.layer_num, sh.head_num, sh.head_dim,
+                             sh.itemsize, sh.page_size, args.pages or sh.num_pages)
+        L, R, ps, P = sh.layer_num, sh.row_bytes, sh.page_size, sh.num_pages
+        desc = gt.make_desc(L, sh.head_num, sh.head_dim, sh.itemsize, ps, P)
+        total, pad = gt.kv_pool_required_bytes(desc)
+        free, _ = torch.cuda.mem_get_info(dev)
+        if total + pad + (8 << 30) > free:
+            print(json.dumps({"micro": "skipped", "cfg": cfg, "reason": f"{free / 2**30:.1f} GiB free"}))
+            continue
+        raw = torch.empty(total + pad, dtype=torch.uint8, device=dev)
+        synth.fill_sentinel_torch(raw, 99)
+        pool = gt.kv_pool_create(desc, raw)
+
+        def d(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+        slots = synth.store_slots(sh, 0)
+        n = slots.size
+        n_tomb = int(np.count_nonzero(slots < 0))
+        slots_d = d(slots)
+        ids = torch.empty(n, dtype=torch.int32, device=dev)
+        gt.kv_translate(pool, slots_d, ids)
+        calls = args.iters
+        if "translate" in kernels:
+            ms = timed(lambda i: gt.kv_translate(pool, slots_d, ids), calls, True)
+            report("translate", cfg, f"{n} slots", ms, n * 12, n)
+        if "store" in kernels or "store_graph" in kernels:
+            K = _payload_torch(gen, n, R, sh.itemsize, dev)
+            V = _payload_torch(gen, n, R, sh.itemsize, dev)
+            useful = (n - n_tomb) * 4 * R + n * 4
+            flush = useful < 4 * l2
+            if "store" in kernels:
+                ms = timed(lambda i: gt.kv_store_layer(pool, i % L, ids, K, V), max(calls, L), flush)
+                report("store_layer", cfg, f"{n} tokens per layer ({n_tomb} tombstones)", ms, useful, 2 * n,
+                       {"l2_flush": flush, "tombstone_bytes": n_tomb * 4 * R})
+            if "store_graph" in kernels:
+                g = torch.cuda.CUDAGraph()
+                s2 = torch.cuda.Stream(dev)
+                s2.wait_stream(stream)
+                with torch.cuda.stream(s2):
+                    for layer in range(L):
+                        gt.kv_store_layer(pool, layer, ids, K, V)
+                stream.wait_stream(s2)
+                with torch.cuda.graph(g):
+                    for layer in range(L):
+                        gt.kv_store_layer(pool, layer, ids, K, V)
+                ms = timed(lambda i: g.replay(), calls, L * useful < 4 * l2)
+                report("store_layer_x32_graph", cfg, f"{L} per-layer stores of {n} tokens in one CUDA graph",
+                       ms, L * useful, 2 * n * L, {"l2_flush": L * useful < 4 * l2})
+                del g
+            del K, V
+        if "store_all" in kernels:
+            na = n if cfg != 2 else 256
+            Ka = _payload_torch(gen, L * na, R, sh.itemsize, dev)
+            Va = _payload_torch(gen, L * na, R, sh.itemsize, dev)
+            ta = int(np.count_nonzero(slots[:na] < 0))
+            useful = L * (na - ta) * 4 * R + na * 4
+            flush = useful < 4 * l2
+            ms = timed(lambda i: gt.kv_store_all_layers(pool, ids[:na], Ka, Va), calls, flush)
+            report("store_all_layers", cfg, f"{na} tokens x {L} layers", ms, useful, 2 * L * na,
+                   {"l2_flush": flush})
+            del Ka, Va
+        if "gather" in kernels:
+            gb = synth.gather_batch(sh) if not args.seqs else synth.GatherBatch(
+                synth.gather_batch(sh).block_table[: args.seqs], np.zeros(args.seqs, np.int32),
+                synth.gather_batch(sh).seq_len[: args.seqs])
+            rows = gb.total
+            ok = torch.empty((rows, R), dtype=torch.uint8, device=dev)
+            ov = torch.empty_like(ok)
+            bt, ln, cu, st = d(gb.block_table), d(gb.seq_len), d(gb.cu), d(gb.seq_start)
+            useful = rows * 4 * R + rows * 4 // ps
+            flush = useful < 4 * l2
+            layers = list(range(L)) if cfg != 5 else [0, L - 1]
+            ms = timed(lambda i: gt.kv_gather_layer(pool, layers[i % len(layers)], bt, ln, cu, ok, ov, st),
+                       max(calls, len(layers)), flush)
+            distinct = len(np.unique(gb.block_table))
+            report("gather_layer", cfg, f"{gb.block_table.shape[0]} seqs, {rows} rows", ms, useful, rows,
+                   {"l2_flush": flush, "distinct_pages": distinct,
+                    "page_reads_per_distinct_page": round(gb.block_table.size / max(1, distinct), 2)})
+            del ok, ov
+        if "move" in kernels:
+            src, dst = synth.move_slots(sh)
+            m = src.size
+            mv = torch.empty(2 * m, dtype=torch.int32, device=dev)
+            gt.kv_translate(pool, d(np.concatenate([src, dst])), mv)
+            useful = m * (2 * L * R * 2 + 8)
+            flush = useful < 4 * l2
+            ms = timed(lambda i: gt.kv_move(pool, mv[:m], mv[m:]), calls, flush)
+            report("move", cfg, f"{m} tokens x {2 * L} row-blocks", ms, useful, 2 * L * m, {"l2_flush": flush})
+        err = gt.kv_pool_last_error(pool)
+        assert err == 0, f"device error bits {err}"
+        gt.kv_pool_destroy(pool)
+        del raw
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,7 +627,16 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--micro", action="store_true", help="per-kernel table instead of the step")
+    ap.add_argument("--only", default="", help="micro entries, e.g. gather:2,move:4")
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--pages", type=int, default=0, help="micro: override the page count")
+    ap.add_argument("--layers", type=int, default=0, help="micro: override the layer count")
+    ap.add_argument("--seqs", type=int, default=0, help="micro: gather only the first N sequences")
     args = ap.parse_args()
+    if args.micro:
+        run_micro(args)
+        return
     if args.warmup < 3 and args.impl != "reference":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

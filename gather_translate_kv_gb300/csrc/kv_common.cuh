@@ -40,19 +40,48 @@ __device__ __forceinline__ int64_t div_ps(const DevPool& p, int64_t j) {
 // ---- 16-byte loads / stores with explicit cache behaviour ---------------
 
 enum : int {
-  kLdNc = 0,     // read-only for the whole kernel: non-coherent path, no L1 allocation
-  kLdPlain = 1,  // buffer is also written by the kernel (move): coherent load, no L1 allocation
+  kLdNc = 0,      // read-only for the whole kernel: non-coherent path, no L1 allocation
+  kLdPlain = 1,   // buffer is also written by the kernel (move): coherent load, no L1 allocation
+  kLdNcKeep = 2,  // as kLdNc, and ask L2 to keep the line (evict_last): rows other warps re-read
+  kLdNcFirst = 3, // as kLdNc, and let L2 drop the line first (evict_first): rows read once
+  kLdNcPf = 4,    // as kLdNc, with a 256-byte L2 prefetch hint
 };
 enum : int {
   kStPlain = 0,   // write-back store
-  kStStream = 1,  // evict-first store for outputs the kernel never reads back
+  kStStream = 1,  // st.cs: streaming store for outputs the kernel never reads back
+  kStFirst = 2,   // write-back store with an L2 evict_first hint
 };
 
+// L2 cache-policy operands for the .L2::cache_hint forms.
+struct L2Policy {
+  uint64_t keep;   // evict_last
+  uint64_t first;  // evict_first
+};
+
+__device__ __forceinline__ L2Policy make_l2_policy() {
+  L2Policy c;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(c.keep));
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(c.first));
+  return c;
+}
+
 template <int LD>
-__device__ __forceinline__ uint4 ld16(const uint4* p) {
+__device__ __forceinline__ uint4 ld16(const uint4* p, const L2Policy& pol) {
   uint4 v;
   if constexpr (LD == kLdNc) {
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+  } else if constexpr (LD == kLdNcKeep) {
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(pol.keep));
+  } else if constexpr (LD == kLdNcFirst) {
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(pol.first));
+  } else if constexpr (LD == kLdNcPf) {
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(p));
   } else {
@@ -65,9 +94,13 @@ __device__ __forceinline__ uint4 ld16(const uint4* p) {
 }
 
 template <int ST>
-__device__ __forceinline__ void st16(uint4* p, const uint4& v) {
+__device__ __forceinline__ void st16(uint4* p, const uint4& v, const L2Policy& pol) {
   if constexpr (ST == kStStream) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  } else if constexpr (ST == kStFirst) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol.first)
                  : "memory");
   } else {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -84,20 +117,20 @@ __device__ __forceinline__ void st16(uint4* p, const uint4& v) {
 // chunks of 4 vectors per lane.
 template <int G, int VPL, int N, int LD, int ST>
 __device__ __forceinline__ void copy_rows(const uint4* const (&src)[N], uint4* const (&dst)[N],
-                                          const bool (&go)[N], int g, int64_t vpr) {
+                                          const bool (&go)[N], int g, int64_t vpr, const L2Policy& pol) {
   if constexpr (VPL > 0) {
     uint4 buf[N][VPL];
 #pragma unroll
     for (int i = 0; i < N; ++i)
       if (go[i]) {
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) buf[i][v] = ld16<LD>(src[i] + g + v * G);
+        for (int v = 0; v < VPL; ++v) buf[i][v] = ld16<LD>(src[i] + g + v * G, pol);
       }
 #pragma unroll
     for (int i = 0; i < N; ++i)
       if (go[i]) {
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) st16<ST>(dst[i] + g + v * G, buf[i][v]);
+        for (int v = 0; v < VPL; ++v) st16<ST>(dst[i] + g + v * G, buf[i][v], pol);
       }
   } else {
     static_assert(G == 32, "dynamic rows use whole warps");
@@ -110,17 +143,34 @@ __device__ __forceinline__ void copy_rows(const uint4* const (&src)[N], uint4* c
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int64_t c = c0 + g + 32 * k;
-          if (c < vpr) buf[k] = ld16<LD>(src[i] + c);
+          if (c < vpr) buf[k] = ld16<LD>(src[i] + c, pol);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int64_t c = c0 + g + 32 * k;
-          if (c < vpr) st16<ST>(dst[i] + c, buf[k]);
+          if (c < vpr) st16<ST>(dst[i] + c, buf[k], pol);
         }
       }
     }
   }
 }
+
+// Cache behaviour of each kernel (measured choices; see the per-kernel notes).
+#ifndef GTKV_GATHER_LD
+#define GTKV_GATHER_LD kLdNc
+#endif
+#ifndef GTKV_GATHER_ST
+#define GTKV_GATHER_ST kStStream
+#endif
+#ifndef GTKV_STORE_LD
+#define GTKV_STORE_LD kLdNc
+#endif
+#ifndef GTKV_STORE_ST
+#define GTKV_STORE_ST kStPlain
+#endif
+#ifndef GTKV_MOVE_ST
+#define GTKV_MOVE_ST kStPlain
+#endif
 
 // Row geometry chosen on the host from R/16; the list of instantiations.
 enum class RowKind { V4, V8, V16, V32, V64, V128, V256, Dyn };

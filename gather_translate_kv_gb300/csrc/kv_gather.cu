@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kBlock) k_gather(DevPool p, int32_t layer, con
   const int64_t warp = tid >> 5;
   const int64_t nwarps = nthreads >> 5;
   const int64_t koff = 2 * static_cast<int64_t>(layer) * ps;
+  const L2Policy pol = make_l2_policy();
 
   for (int64_t r0 = warp * 32; r0 < total; r0 += nwarps * 32) {
     // lane's output row -> K-view source row (or -1: leave the row alone)
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kBlock) k_gather(DevPool p, int32_t layer, con
         dst[2 * u] = out_k + o_ * vpr;
         dst[2 * u + 1] = out_v + o_ * vpr;
       }
-      copy_rows<G, VPL, 2 * U, kLdNc, kStStream>(src, dst, go, g, vpr);
+      copy_rows<G, VPL, 2 * U, GTKV_GATHER_LD, GTKV_GATHER_ST>(src, dst, go, g, vpr, pol);
     }
   }
 }

@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(kBlock) k_move(DevPool p, const int32_t* __res
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t blocks = p.blocks;
+  const L2Policy pol = make_l2_policy();
 
   for (int64_t t0 = warp * TPU; t0 < n_tasks; t0 += nwarps * TPU) {
     const uint4* src[U];
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(kBlock) k_move(DevPool p, const int32_t* __res
       src[u] = p.base + (sr >= 0 ? sr : 0) * vpr;
       dst[u] = p.base + (sr >= 0 ? dr : 0) * vpr;
     }
-    copy_rows<G, VPL, U, kLdPlain, kStPlain>(src, dst, go, g, vpr);
+    copy_rows<G, VPL, U, kLdPlain, GTKV_MOVE_ST>(src, dst, go, g, vpr, pol);
   }
 }
 

@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(kBlock) k_store(DevPool p, int32_t layer0, int
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const bool one_layer = n_tasks == n;
+  const L2Policy pol = make_l2_policy();
 
   for (int64_t t0 = warp * TPU; t0 < n_tasks; t0 += nwarps * TPU) {
     const uint4* src[2 * U];
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(kBlock) k_store(DevPool p, int32_t layer0, int
       dst[2 * u] = p.base + rr * vpr;
       dst[2 * u + 1] = p.base + (rr + p.ps) * vpr;
     }
-    copy_rows<G, VPL, 2 * U, kLdNc, kStPlain>(src, dst, go, g, vpr);
+    copy_rows<G, VPL, 2 * U, GTKV_STORE_LD, GTKV_STORE_ST>(src, dst, go, g, vpr, pol);
   }
 }
 

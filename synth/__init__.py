@@ -120,19 +120,20 @@ def _i64(v: int) -> int:
     return v - (1 << 64) if v >= (1 << 63) else v
 
 
-def fill_sentinel_torch(buf, fill_seed: int, chunk_words: int = 1 << 26) -> None:
+def fill_sentinel_torch(buf, fill_seed: int, chunk_words: int = 1 << 26, byte_offset: int = 0) -> None:
     """Fill a uint8 torch tensor (any device, contiguous, length % 8 == 0)
-    with the sentinel pattern, in place, chunk by chunk."""
+    with the sentinel pattern, in place, chunk by chunk. ``byte_offset``
+    (a multiple of 8) is the pattern offset of buf[0]."""
     import torch
 
-    assert buf.dtype == torch.uint8 and buf.is_contiguous() and buf.numel() % 8 == 0
+    assert buf.dtype == torch.uint8 and buf.is_contiguous() and buf.numel() % 8 == 0 and byte_offset % 8 == 0
     words = buf.view(torch.int64)
     n = words.numel()
     inc, m1, m2 = _i64(0x9E3779B97F4A7C15), _i64(0xBF58476D1CE4E5B9), _i64(0x94D049BB133111EB)
     mask = {k: (1 << (64 - k)) - 1 for k in (30, 27, 31)}
     for w0 in range(0, n, chunk_words):
         w1 = min(n, w0 + chunk_words)
-        z = torch.arange(w0, w1, dtype=torch.int64, device=buf.device)
+        z = torch.arange(w0 + byte_offset // 8, w1 + byte_offset // 8, dtype=torch.int64, device=buf.device)
         z.bitwise_xor_(int(fill_seed))
         z.add_(inc)
         z.bitwise_xor_(torch.bitwise_right_shift(z, 30).bitwise_and_(mask[30])).mul_(m1)

@@ -1,0 +1,264 @@
+"""GPU parity at the workloads' full sizes (8 GiB to 119 GiB pools).
+
+No host mirror fits, so the oracle runs in address mode: for every row a call
+writes or reads it names the pool byte offset (its envelope decomposition),
+and the test checks on the device, with plain torch indexing, that
+  * every row a store writes holds that input row at the oracle's offset,
+  * every gathered row equals the content at the oracle's source offset
+    (the sentinel pattern, or the row a store put there),
+  * every moved row equals the source row's content,
+  * no other row of the pool (nor its tail pad) changed: the set of rows
+    that differ from the sentinel is exactly the set the oracle predicts.
+Every output row is checked, not a sample. Tombstoned tokens go to the sink
+rows, which follow the sink rule of gpu_util.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import gather_translate_kv_gb300 as gt
+import oracle
+import synth
+from gpu_util import as_rows, dev_bits
+
+pytestmark = pytest.mark.gpu
+
+FILL = 31337
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gather_translate_kv_gb300 import build
+
+    build.build()
+    oracle.build()
+
+
+class Full:
+    """A full-size device pool filled with the sentinel, and its oracle."""
+
+    def __init__(self, shape: synth.Shape):
+        self.shape = shape
+        self.o = oracle.Oracle(oracle.Geometry(shape.layer_num, shape.head_num, shape.head_dim, shape.itemsize,
+                                               shape.page_size, shape.num_pages))
+        self.sizes = self.o.sizes()
+        self.R = self.sizes["row_bytes"]
+        nbytes = self.o.raw_bytes()
+        free, _ = torch.cuda.mem_get_info()
+        if nbytes + (12 << 30) > free:
+            pytest.skip(f"skipped: {free / 2**30:.1f} GiB free, the {shape.name} pool needs {nbytes / 2**30:.1f} GiB")
+        self.raw = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        synth.fill_sentinel_torch(self.raw, FILL)
+        self.rows = self.raw.view(-1, self.R)  # anchor 0: every row offset is a multiple of R
+        self.pool = gt.kv_pool_create(gt.make_desc(shape.layer_num, shape.head_num, shape.head_dim, shape.itemsize,
+                                                   shape.page_size, shape.num_pages), self.raw)
+        self.written = []  # row indices (offset // R) the oracle says were written
+        self.sinks = {self.o.slot_row_byte(0, b) // self.R for b in range(2 * shape.layer_num)}
+
+    def close(self):
+        gt.kv_pool_destroy(self.pool)
+        del self.rows, self.raw
+        torch.cuda.empty_cache()
+
+    def translate(self, slots: np.ndarray) -> torch.Tensor:
+        ids = torch.empty(slots.size, dtype=torch.int32, device="cuda")
+        gt.kv_translate(self.pool, torch.from_numpy(slots).cuda(), ids)
+        return ids
+
+    def sentinel(self, offsets: np.ndarray) -> torch.Tensor:
+        return synth.sentinel_rows_torch(FILL, torch.from_numpy(offsets).cuda(), self.R)
+
+    def check_store(self, layer, slots, K, V, ids=None):
+        """Store one layer through the C ABI and check every written row."""
+        kd, vd, err = self.o.store_rows(layer, slots)
+        ids = self.translate(slots) if ids is None else ids
+        Kd, Vd = torch.from_numpy(as_rows(K, self.R)).cuda(), torch.from_numpy(as_rows(V, self.R)).cuda()
+        gt.kv_store_layer(self.pool, layer, ids, Kd, Vd)
+        assert gt.kv_pool_last_error(self.pool) == dev_bits(err) == 0
+        self._check_rows(slots, kd, vd, Kd, Vd)
+        return kd, vd, Kd, Vd
+
+    def _check_rows(self, slots, kd, vd, Kd, Vd):
+        live = torch.from_numpy(np.nonzero(slots >= 0)[0]).cuda()
+        for off, src in ((kd, Kd), (vd, Vd)):
+            idx = torch.from_numpy(off // self.R).cuda()
+            got = self.rows[idx[live]]
+            assert torch.equal(got, src[live]), "stored rows differ from the inputs at the oracle's offsets"
+            self.written.append(idx[live])
+
+    def check_untouched(self, chunk_rows: int = 1 << 22):
+        """Rows that differ from the sentinel == rows the oracle says were
+        written (sink rows aside); the tail pad never differs."""
+        want = torch.unique(torch.cat(self.written)) if self.written else \
+            torch.zeros(0, dtype=torch.int64, device="cuda")
+        n = self.rows.shape[0]
+        buf = torch.empty(min(chunk_rows, n) * self.R, dtype=torch.uint8, device="cuda")
+        got = []
+        for r0 in range(0, n, chunk_rows):
+            r1 = min(n, r0 + chunk_rows)
+            b = buf[: (r1 - r0) * self.R]
+            synth.fill_sentinel_torch(b, FILL, byte_offset=r0 * self.R)
+            diff = (self.rows[r0:r1] != b.view(-1, self.R)).any(dim=1)
+            got.append(torch.nonzero(diff).flatten() + r0)
+        got = torch.cat(got)
+        if self.sinks:
+            sinks = torch.tensor(sorted(self.sinks), device="cuda")
+            got = got[~torch.isin(got, sinks)]
+            want = want[~torch.isin(want, sinks)]
+        n_pool_rows = self.sizes["total"] // self.R
+        assert int((got >= n_pool_rows).sum()) == 0, "the tail pad changed"
+        assert got.numel() == want.numel() and torch.equal(got, want), \
+            f"{got.numel()} rows changed, the oracle predicts {want.numel()}"
+
+    def expected_reads(self, offsets: np.ndarray, stored: list) -> torch.Tensor:
+        """Content at byte offsets: the sentinel, or the row a store put there.
+        `stored` = [(offsets int64[n], rows uint8[n, R] on the device)]."""
+        exp = self.sentinel(offsets)
+        offs_d = torch.from_numpy(offsets).cuda()
+        for so, srows in stored:
+            so_d = torch.from_numpy(so).cuda()
+            order = torch.argsort(so_d)
+            so_s = so_d[order]
+            pos = torch.searchsorted(so_s, offs_d).clamp_(max=max(0, so_s.numel() - 1))
+            hit = so_s[pos] == offs_d if so_s.numel() else torch.zeros_like(offs_d, dtype=torch.bool)
+            exp[hit] = srows[order[pos[hit]]]
+        return exp
+
+    def check_gather(self, layer, gb: synth.GatherBatch, stored: list):
+        ks, vs, err = self.o.gather_rows(layer, gb.block_table, gb.seq_len, gb.cu, gb.seq_start)
+        assert err == 0 and (ks >= 0).all()
+        d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        ok = torch.empty((gb.total, self.R), dtype=torch.uint8, device="cuda")
+        ov = torch.empty_like(ok)
+        gt.kv_gather_layer(self.pool, layer, d(gb.block_table), d(gb.seq_len), d(gb.cu), ok, ov, d(gb.seq_start))
+        assert gt.kv_pool_last_error(self.pool) == 0
+        assert torch.equal(ok, self.expected_reads(ks, stored[0])), f"gathered K of layer {layer} differs"
+        assert torch.equal(ov, self.expected_reads(vs, stored[1])), f"gathered V of layer {layer} differs"
+
+
+def _vals(shape, n, layer, seed_extra=0):
+    return synth.kv_pair(shape, n, layer, seed=shape.seed + seed_extra)
+
+
+def test_decode_llama3_8b_full():
+    """Workload 2 (8 GiB pool): gathers of 256 x 4096 tokens on the fresh
+    pool, the per-layer decode store for all 32 layers, gathers that read the
+    new tokens, and the 8192-token move."""
+    sh = synth.SHAPES[2]
+    F = Full(sh)
+    gb = synth.gather_batch(sh)
+    for layer in (0, 31):
+        F.check_gather(layer, gb, ([], []))
+    stored = {}
+    for layer in range(sh.layer_num):
+        slots = synth.store_slots(sh, layer)
+        K, V = _vals(sh, slots.size, layer)
+        kd, vd, Kd, Vd = F.check_store(layer, slots, K, V)
+        stored[layer] = ((kd, Kd), (vd, Vd))
+    for layer in (0, 17, 31):
+        F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]))
+    # move 8192 never-stored tokens to other never-stored tokens
+    used = np.unique(np.concatenate([synth.store_slots(sh, l) for l in range(sh.layer_num)]))
+    src, dst = synth.move_slots(sh, 8192, avoid=used)
+    src = np.setdiff1d(src, used)[:8000]
+    dst = dst[: src.size]
+    sb, db, err = F.o.move_rows(*[F.o.translate(x)[0] for x in (src, dst)])
+    assert err == 0
+    gt.kv_move(F.pool, F.translate(src), F.translate(dst))
+    assert gt.kv_pool_last_error(F.pool) == 0
+    assert torch.equal(F.rows[torch.from_numpy(db // F.R).cuda()], F.sentinel(sb)), "moved rows differ"
+    F.written.append(torch.from_numpy(db // F.R).cuda())
+    F.check_untouched()
+    F.close()
+
+
+def test_prefill_llama3_8b_full():
+    """Workload 3 (32 GiB pool): 32 per-layer stores of 32768 prefill tokens
+    with 2% tombstones, then on a fresh pool the all-layer store of
+    [32, 32768, 8, 128] K and V, then gathers of the 16 prefill sequences."""
+    sh = synth.SHAPES[3]
+    slots, pages = synth.prefill_slots(sh)
+    F = Full(sh)
+    for layer in range(sh.layer_num):
+        K, V = _vals(sh, slots.size, layer)
+        F.check_store(layer, slots, K, V)
+    F.check_untouched()
+    F.close()
+    F = Full(sh)
+    Ka, Va = synth.kv_pair_all(sh, slots.size)
+    ids = F.translate(slots)
+    Kd = torch.from_numpy(Ka.view(np.uint8)).cuda().view(sh.layer_num, slots.size, F.R)
+    Vd = torch.from_numpy(Va.view(np.uint8)).cuda().view(sh.layer_num, slots.size, F.R)
+    gt.kv_store_all_layers(F.pool, ids, Kd, Vd)
+    assert gt.kv_pool_last_error(F.pool) == 0
+    gb = synth.gather_batch(sh)
+    for layer in range(sh.layer_num):
+        kd, vd, err = F.o.store_rows(layer, slots)
+        assert err == 0
+        F._check_rows(slots, kd, vd, Kd[layer], Vd[layer])
+        if layer in (0, 31):
+            live = slots >= 0
+            F.check_gather(layer, gb, ([(kd[live], Kd[layer][torch.from_numpy(live).cuda()])],
+                                       [(vd[live], Vd[layer][torch.from_numpy(live).cuda()])]))
+    F.check_untouched()
+    F.close()
+
+
+def test_swa_fp8_full():
+    """Workload 4 (12 GiB fp8 pool): for each of the 24 layers, store one
+    token per sequence at position c-1 and gather the 128-token window
+    [c-128, c) of all 512 sequences; then the 8192-token move."""
+    sh = synth.SHAPES[4]
+    F = Full(sh)
+    slots, gb = synth.swa_batch(sh)
+    ids = F.translate(slots)
+    for layer in range(sh.layer_num):
+        K, V = _vals(sh, slots.size, layer)
+        kd, vd, Kd, Vd = F.check_store(layer, slots, K, V, ids)
+        F.check_gather(layer, gb, ([(kd, Kd)], [(vd, Vd)]))
+    used = np.unique(gb.block_table.astype(np.int64)[:, :, None] * sh.page_size + np.arange(sh.page_size))
+    src, dst = synth.move_slots(sh, 8192, avoid=used)
+    src = np.setdiff1d(src, used)[:8000]
+    dst = dst[: src.size]
+    sb, db, err = F.o.move_rows(*[F.o.translate(x)[0] for x in (src, dst)])
+    assert err == 0
+    gt.kv_move(F.pool, F.translate(src), F.translate(dst))
+    assert gt.kv_pool_last_error(F.pool) == 0
+    assert torch.equal(F.rows[torch.from_numpy(db // F.R).cuda()], F.sentinel(sb))
+    F.written.append(torch.from_numpy(db // F.R).cuda())
+    F.check_untouched()
+    F.close()
+
+
+def test_id_bound_stress_full():
+    """Workload 5 (119.2 GiB fp8 pool, 1 999 994 880 kernel rows, just under
+    2^31): 1M-token stores into all 80 layers (slots include every slot of
+    the last 4 pages), 1M-row gathers of layers 0 and 79, the id of the last
+    slot, and the id-bound rejection one page further."""
+    sh = synth.SHAPES[5]
+    d_bad = gt.make_desc(sh.layer_num, sh.head_num, sh.head_dim, sh.itemsize, sh.page_size, 52429)
+    with pytest.raises(gt.KVError) as e:
+        gt.kv_pool_create(d_bad)  # rejected on the host, nothing allocated
+    assert e.value.name == "KV_ERR_ID_BOUND"
+    F = Full(sh)
+    assert F.sizes["n_rows"] == 1_999_994_880
+    last = np.array([sh.num_pages * sh.page_size - 1], np.int64)
+    assert int(F.translate(last).item()) == 1_999_954_175
+    stored = {}
+    for layer in range(sh.layer_num):
+        slots = synth.store_slots(sh, layer)
+        assert slots.max() == sh.num_pages * sh.page_size - 1
+        K, V = _vals(sh, slots.size, layer)
+        kd, vd, Kd, Vd = F.check_store(layer, slots, K, V)
+        if layer in (0, 79):
+            stored[layer] = ((kd, Kd), (vd, Vd))
+    gb = synth.gather_batch(sh)
+    assert (gb.block_table == sh.num_pages - 1).any()
+    for layer in (0, 79):
+        F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]))
+    F.check_untouched()
+    F.close()

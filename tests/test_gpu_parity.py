@@ -52,10 +52,16 @@ SHAPES = [
 IDS = [f"{s.name}-R{s.row_bytes}-ps{s.page_size}" for s, _ in SHAPES]
 
 
+def _store_pages(shape: synth.Shape) -> int:
+    """Stores use pages [1, hi); pages [hi, P) stay free for move destinations."""
+    return max(2, (2 * shape.num_pages) // 3)
+
+
 def _tokens(shape: synth.Shape, rng, n: int, tomb: int) -> np.ndarray:
-    ps, P = shape.page_size, shape.num_pages
-    n = min(n, (P - 1) * ps)
-    slots = synth.distinct_slots(rng, ps, P * ps, n)
+    ps = shape.page_size
+    hi = _store_pages(shape)
+    n = min(n, (hi - 1) * ps)
+    slots = synth.distinct_slots(rng, ps, hi * ps, n)
     return synth.with_tombstones(rng, slots, min(tomb, n))
 
 
@@ -184,12 +190,11 @@ def test_path_matches_oracle(shape, anchor):
             assert_bytes_equal(dv.cpu().numpy(), ov, f"gather V layer {layer}", R)
 
     # move: stored tokens -> never-stored tokens (disjoint, distinct)
-    if shape.cfg == 1:
-        src_slots = rng.choice(sorted(stored), size=20, replace=False).astype(np.int64)
-    else:
-        src_slots = rng.choice(sorted(stored), size=min(len(stored), 150), replace=False).astype(np.int64)
     free = np.setdiff1d(np.arange(ps, P * ps, dtype=np.int64), np.array(sorted(stored), np.int64))
-    dst_slots = rng.choice(free, size=src_slots.size, replace=False).astype(np.int64)
+    m = min(20 if shape.cfg == 1 else 150, len(stored), free.size)
+    assert m >= 10, "test setup leaves too few free slots"
+    src_slots = rng.choice(sorted(stored), size=m, replace=False).astype(np.int64)
+    dst_slots = rng.choice(free, size=m, replace=False).astype(np.int64)
     src_ids, _ = o.translate(src_slots)
     dst_ids, _ = o.translate(dst_slots)
     err = o.move(pp.M, src_ids, dst_ids)
