@@ -156,24 +156,34 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
-def profiled_traffic(kernel_source: str):
-    """DRAM bytes per gather launch from the committed ncu summary, or None when
-    the kernel source changed since the counters were taken."""
+GATHER_SOURCES = [os.path.join(ROOT, "gather_translate_kv_gb300", "csrc", f) for f in ("kv_gather.cu", "kv_common.cuh")]
+
+
+def sources_hash(paths) -> str:
+    """Short hash of the sources a kernel is built from."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", "gather_decode_llama3_8b.txt")
+    h = hashlib.sha256()
+    for path in paths:
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary="gather_decode_llama3_8b.txt", sources=GATHER_SOURCES):
+    """DRAM bytes per gather launch from the committed ncu summary, or None when
+    the kernel's sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", summary)
     try:
         text = open(path).read()
     except OSError:
         return None
-    want = hashlib.sha256(open(kernel_source, "rb").read()).hexdigest()[:16]
     src_hash = traffic = None
     for line in text.splitlines():
-        if line.startswith("kernel_source_sha256_16:"):
+        if line.startswith("kernel_sources_sha256_16:"):
             src_hash = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_full_launch:"):
+        if line.startswith("dram_bytes_per_launch:"):
             traffic = float(line.split(":", 1)[1].strip())
-    return traffic if src_hash == want else None
+    return traffic if src_hash == sources_hash(sources) else None
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -375,7 +385,7 @@ def run_gpu(args):
     peak, peak_kind = measured_hbm_peak()
     gather_bytes = ub["gather"] / L
     achieved = gather_bytes / (gather_ms * 1e-3) / GB
-    traffic = profiled_traffic(os.path.join(ROOT, "gather_translate_kv_gb300", "csrc", "kv_gather.cu"))
+    traffic = profiled_traffic()
     line = {
         "metric": "KV store/gather/move useful GB/s and % of GB300 HBM peak (byte-exact vs oracle)",
         "value": round(whole_job_gbps(step_bytes, world, ms), 1),
@@ -442,10 +452,10 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ per-kernel table
 
-MICRO_DEFAULT = ["translate:2", "store:2", "store_graph:2", "store_all:2", "gather:2", "move:2",
-                 "translate:3", "store:3", "store_all:3", "gather:3",
+MICRO_DEFAULT = ["translate:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2", "move:2",
+                 "translate:3", "store:3", "store_slots:3", "store_all:3", "gather:3",
                  "store:4", "gather:4", "move:4",
-                 "translate:5", "store:5", "gather:5", "move:5"]
+                 "translate:5", "store:5", "store_slots:5", "gather:5", "move:5"]
 
 
 def _payload_torch(gen, rows: int, R: int, itemsize: int, dev):
@@ -510,13 +520,20 @@ def run_micro(args):
                 ms.append(e0.elapsed_time(e1))
         return ms
 
-    def report(kernel, cfg, workload, ms, useful, rows, extra=None):
-        med = statistics.median(ms)
+    def report(kernel, cfg, workload, ms, useful, rows, extra=None, ref_ms=None):
+        # the event clock ticks in ~2 us steps on this part: the mean over many
+        # launches resolves short kernels better than the median
+        med = statistics.mean(ms)
         line = {"micro": kernel, "cfg": cfg, "workload": workload, "calls": len(ms),
-                "us_per_call": round(med * 1e3, 2), "useful_bytes_per_call": useful,
+                "us_per_call": round(med * 1e3, 2), "us_median": round(statistics.median(ms) * 1e3, 2),
+                "useful_bytes_per_call": useful,
                 "useful_GBps": round(useful / (med * 1e-3) / GB, 1),
                 "pct_of_hbm_peak": round(100 * useful / (med * 1e-3) / GB / peak, 1),
                 "rows_per_s": round(rows / (med * 1e-3), 1), "peak_GBps": peak, "peak_source": peak_kind}
+        if ref_ms:
+            r = statistics.mean(ref_ms)
+            line["torch_indexing_us"] = round(r * 1e3, 2)
+            line["speedup_vs_torch_indexing"] = round(r / med, 2)
         line.update(extra or {})
         print(json.dumps(line), flush=True)
 
@@ -539,6 +556,14 @@ def run_micro(args):
         def d(a):
             return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
+        # The report's own method on the same bytes, for comparison: dense
+        # per-layer views over the raw buffer (build_mha_views: block b starts
+        # at b*ps*R, rows of R bytes) and torch indexing through them.
+        n_rows_view = P * 2 * L * ps
+
+        def view(block):
+            return torch.as_strided(raw, size=(n_rows_view, R), stride=(R, 1), storage_offset=block * ps * R)
+
         slots = synth.store_slots(sh, 0)
         n = slots.size
         n_tomb = int(np.count_nonzero(slots < 0))
@@ -549,15 +574,25 @@ def run_micro(args):
         if "translate" in kernels:
             ms = timed(lambda i: gt.kv_translate(pool, slots_d, ids), calls, True)
             report("translate", cfg, f"{n} slots", ms, n * 12, n)
-        if "store" in kernels or "store_graph" in kernels:
+        if "store" in kernels or "store_graph" in kernels or "store_slots" in kernels:
             K = _payload_torch(gen, n, R, sh.itemsize, dev)
             V = _payload_torch(gen, n, R, sh.itemsize, dev)
             useful = (n - n_tomb) * 4 * R + n * 4
             flush = useful < 4 * l2
             if "store" in kernels:
                 ms = timed(lambda i: gt.kv_store_layer(pool, i % L, ids, K, V), max(calls, L), flush)
+                ids64 = ids.to(torch.int64)
+
+                def ref_store(i):
+                    view(2 * (i % L))[ids64] = K
+                    view(2 * (i % L) + 1)[ids64] = V
+                ref = timed(ref_store, max(calls, L), flush) if args.torch_ref else None
                 report("store_layer", cfg, f"{n} tokens per layer ({n_tomb} tombstones)", ms, useful, 2 * n,
-                       {"l2_flush": flush, "tombstone_bytes": n_tomb * 4 * R})
+                       {"l2_flush": flush, "tombstone_bytes": n_tomb * 4 * R}, ref)
+            if "store_slots" in kernels:
+                ms = timed(lambda i: gt.kv_store_layer_slots(pool, i % L, slots_d, K, V), max(calls, L), flush)
+                report("store_layer_slots", cfg, f"{n} slots per layer, translate fused ({n_tomb} tombstones)",
+                       ms, useful + n * 4, 2 * n, {"l2_flush": flush})
             if "store_graph" in kernels:
                 g = torch.cuda.CUDAGraph()
                 s2 = torch.cuda.Stream(dev)
@@ -598,10 +633,22 @@ def run_micro(args):
             layers = list(range(L)) if cfg != 5 else [0, L - 1]
             ms = timed(lambda i: gt.kv_gather_layer(pool, layers[i % len(layers)], bt, ln, cu, ok, ov, st),
                        max(calls, len(layers)), flush)
+            ref = None
+            if args.torch_ref:
+                # view rows of every output token, precomputed (not timed)
+                seq = np.repeat(np.arange(gb.block_table.shape[0]), gb.seq_len - gb.seq_start)
+                j = np.concatenate([np.arange(a, b) for a, b in zip(gb.seq_start, gb.seq_len)])
+                vrow = torch.from_numpy(gb.block_table[seq, j // ps].astype(np.int64) * (2 * L * ps) + j % ps).to(dev)
+
+                def ref_gather(i):
+                    layer = layers[i % len(layers)]
+                    torch.index_select(view(2 * layer), 0, vrow, out=ok)
+                    torch.index_select(view(2 * layer + 1), 0, vrow, out=ov)
+                ref = timed(ref_gather, max(calls, len(layers)), flush)
             distinct = len(np.unique(gb.block_table))
             report("gather_layer", cfg, f"{gb.block_table.shape[0]} seqs, {rows} rows", ms, useful, rows,
                    {"l2_flush": flush, "distinct_pages": distinct,
-                    "page_reads_per_distinct_page": round(gb.block_table.size / max(1, distinct), 2)})
+                    "page_reads_per_distinct_page": round(gb.block_table.size / max(1, distinct), 2)}, ref)
             del ok, ov
         if "move" in kernels:
             src, dst = synth.move_slots(sh)
@@ -611,7 +658,16 @@ def run_micro(args):
             useful = m * (2 * L * R * 2 + 8)
             flush = useful < 4 * l2
             ms = timed(lambda i: gt.kv_move(pool, mv[:m], mv[m:]), calls, flush)
-            report("move", cfg, f"{m} tokens x {2 * L} row-blocks", ms, useful, 2 * L * m, {"l2_flush": flush})
+            ref = None
+            if args.torch_ref:
+                s64, d64 = mv[:m].to(torch.int64), mv[m:].to(torch.int64)
+
+                def ref_move(i):  # every layer's K and V view, one indexing op each
+                    for b in range(2 * L):
+                        vb = view(b)
+                        vb[d64] = vb[s64]
+                ref = timed(ref_move, max(3, calls // 4), flush)
+            report("move", cfg, f"{m} tokens x {2 * L} row-blocks", ms, useful, 2 * L * m, {"l2_flush": flush}, ref)
         err = gt.kv_pool_last_error(pool)
         assert err == 0, f"device error bits {err}"
         gt.kv_pool_destroy(pool)
@@ -629,7 +685,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--micro", action="store_true", help="per-kernel table instead of the step")
     ap.add_argument("--only", default="", help="micro entries, e.g. gather:2,move:4")
-    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--iters", type=int, default=50)
+    ap.add_argument("--torch-ref", type=int, default=1, help="micro: also time torch indexing through dense views")
     ap.add_argument("--pages", type=int, default=0, help="micro: override the page count")
     ap.add_argument("--layers", type=int, default=0, help="micro: override the layer count")
     ap.add_argument("--seqs", type=int, default=0, help="micro: gather only the first N sequences")

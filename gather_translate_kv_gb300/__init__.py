@@ -102,8 +102,11 @@ def lib():
         "kv_translate": [vp, vp, i64, vp, i64, vp, vp],
         "kv_store_layer": [vp, i32, vp, i64, vp, vp, vp],
         "kv_store_all_layers": [vp, vp, i64, vp, vp, vp],
+        "kv_store_layer_slots": [vp, i32, vp, i64, vp, i64, vp, vp, vp],
+        "kv_store_all_layers_slots": [vp, vp, i64, vp, i64, vp, vp, vp],
         "kv_gather_layer": [vp, i32, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
         "kv_move": [vp, vp, vp, i64, vp],
+        "kv_translate_block_table": [vp, vp, i32, i32, vp, vp, i64, vp, vp],
         "kv_pool_last_error": [vp, vp, P(i32)],
     }
     for name, args in sig.items():
@@ -229,6 +232,25 @@ def kv_store_all_layers(pool: KVPool, ids: torch.Tensor, k_all: torch.Tensor, v_
         _dev(v_all, "v_all", nbytes=nb), _stream(stream)))
 
 
+def kv_store_layer_slots(pool: KVPool, layer: int, slots: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         v2p: torch.Tensor | None = None, stream=None) -> None:
+    n = slots.numel()
+    nb = n * pool.row_bytes
+    _check("kv_store_layer_slots", lib().kv_store_layer_slots(
+        pool.handle, layer, _dev(slots, "slots", torch.int64), n, _dev(v2p, "v2p", torch.int32),
+        0 if v2p is None else v2p.numel(), _dev(k, "k", nbytes=nb), _dev(v, "v", nbytes=nb), _stream(stream)))
+
+
+def kv_store_all_layers_slots(pool: KVPool, slots: torch.Tensor, k_all: torch.Tensor, v_all: torch.Tensor,
+                              v2p: torch.Tensor | None = None, stream=None) -> None:
+    n = slots.numel()
+    nb = pool.desc.layer_num * n * pool.row_bytes
+    _check("kv_store_all_layers_slots", lib().kv_store_all_layers_slots(
+        pool.handle, _dev(slots, "slots", torch.int64), n, _dev(v2p, "v2p", torch.int32),
+        0 if v2p is None else v2p.numel(), _dev(k_all, "k_all", nbytes=nb), _dev(v_all, "v_all", nbytes=nb),
+        _stream(stream)))
+
+
 def kv_gather_layer(pool: KVPool, layer: int, block_table: torch.Tensor, seq_len: torch.Tensor,
                     cu_out: torch.Tensor, out_k: torch.Tensor, out_v: torch.Tensor,
                     seq_start: torch.Tensor | None = None, stream=None) -> None:
@@ -256,6 +278,22 @@ def kv_move(pool: KVPool, src_ids: torch.Tensor, dst_ids: torch.Tensor, stream=N
         raise ValueError("src_ids and dst_ids must have the same length")
     _check("kv_move", lib().kv_move(pool.handle, _dev(src_ids, "src_ids", torch.int32),
                                     _dev(dst_ids, "dst_ids", torch.int32), n, _stream(stream)))
+
+
+def kv_translate_block_table(pool: KVPool, virt_bt: torch.Tensor, seq_len: torch.Tensor, v2p: torch.Tensor,
+                             out_bt: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Prefix-only kernel-facing block table (entries phys * 2L); in place
+    when out_bt is virt_bt or None."""
+    if virt_bt.dim() != 2:
+        raise ValueError("virt_bt must be [n_seqs, max_pages]")
+    n_seqs, max_pages = virt_bt.shape
+    out_bt = virt_bt if out_bt is None else out_bt
+    if out_bt.shape != virt_bt.shape or seq_len.numel() != n_seqs:
+        raise ValueError("out_bt must match virt_bt; seq_len must be [n_seqs]")
+    _check("kv_translate_block_table", lib().kv_translate_block_table(
+        pool.handle, _dev(virt_bt, "virt_bt", torch.int32), n_seqs, max_pages, _dev(seq_len, "seq_len", torch.int32),
+        _dev(v2p, "v2p", torch.int32), v2p.numel(), _dev(out_bt, "out_bt", torch.int32), _stream(stream)))
+    return out_bt
 
 
 def kv_pool_last_error(pool: KVPool, stream=None) -> int:

@@ -198,6 +198,35 @@ int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n
                                      pool->sm_count, as_stream(stream)));
 }
 
+static int store_slots(const kv_pool_t* pool, int32_t layer0, int32_t n_layers, const int64_t* slots_dev, int64_t n,
+                       const int32_t* v2p_dev, int64_t v2p_len, const void* k_dev, const void* v_dev,
+                       kv_stream_t stream) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (n < 0 || v2p_len < 0) return KV_ERR_INVALID;
+  if (n == 0) return KV_OK;
+  if (slots_dev == nullptr || k_dev == nullptr || v_dev == nullptr || (v2p_dev == nullptr && v2p_len > 0))
+    return KV_ERR_INVALID;
+  if (!aligned16(k_dev) || !aligned16(v_dev) || (reinterpret_cast<uintptr_t>(slots_dev) & 7u) ||
+      (reinterpret_cast<uintptr_t>(v2p_dev) & 3u))
+    return KV_ERR_ALIGN;
+  return launched(gtkv::launch_store_slots(pool->dev, layer0, n_layers, slots_dev, n, v2p_dev, v2p_len, k_dev,
+                                           v_dev, pool->sm_count, as_stream(stream)));
+}
+
+int kv_store_layer_slots(const kv_pool_t* pool, int32_t layer, const int64_t* slots_dev, int64_t n,
+                         const int32_t* v2p_dev, int64_t v2p_len, const void* k_dev, const void* v_dev,
+                         kv_stream_t stream) {
+  if (pool != nullptr && (layer < 0 || layer >= pool->desc.layer_num)) return KV_ERR_INVALID;
+  return store_slots(pool, layer, 1, slots_dev, n, v2p_dev, v2p_len, k_dev, v_dev, stream);
+}
+
+int kv_store_all_layers_slots(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int32_t* v2p_dev,
+                              int64_t v2p_len, const void* k_all_dev, const void* v_all_dev, kv_stream_t stream) {
+  if (pool == nullptr) return KV_ERR_INVALID;
+  return store_slots(pool, 0, pool->desc.layer_num, slots_dev, n, v2p_dev, v2p_len, k_all_dev, v_all_dev, stream);
+}
+
 int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_table_dev, int32_t n_seqs,
                     int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
                     const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
@@ -229,6 +258,22 @@ int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* ds
   if ((reinterpret_cast<uintptr_t>(src_ids_dev) & 3u) || (reinterpret_cast<uintptr_t>(dst_ids_dev) & 3u))
     return KV_ERR_ALIGN;
   return launched(gtkv::launch_move(pool->dev, src_ids_dev, dst_ids_dev, n, pool->sm_count, as_stream(stream)));
+}
+
+int kv_translate_block_table(const kv_pool_t* pool, const int32_t* virt_bt_dev, int32_t n_seqs, int32_t max_pages,
+                             const int32_t* seq_len_dev, const int32_t* v2p_dev, int64_t v2p_len,
+                             int32_t* out_bt_dev, kv_stream_t stream) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (n_seqs < 0 || max_pages < 0 || v2p_len < 0) return KV_ERR_INVALID;
+  if (n_seqs == 0 || max_pages == 0) return KV_OK;
+  if (virt_bt_dev == nullptr || seq_len_dev == nullptr || out_bt_dev == nullptr || (v2p_dev == nullptr && v2p_len > 0))
+    return KV_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(virt_bt_dev) & 3u) || (reinterpret_cast<uintptr_t>(out_bt_dev) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_len_dev) & 3u) || (reinterpret_cast<uintptr_t>(v2p_dev) & 3u))
+    return KV_ERR_ALIGN;
+  return launched(gtkv::launch_block_table(pool->dev, virt_bt_dev, n_seqs, max_pages, seq_len_dev, v2p_dev, v2p_len,
+                                           out_bt_dev, pool->sm_count, as_stream(stream)));
 }
 
 int kv_pool_last_error(const kv_pool_t* pool, kv_stream_t stream, int32_t* dev_code) {

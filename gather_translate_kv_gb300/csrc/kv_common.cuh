@@ -37,6 +37,33 @@ __device__ __forceinline__ int64_t div_ps(const DevPool& p, int64_t j) {
   return p.ps_shift >= 0 ? (j >> p.ps_shift) : j / p.ps;
 }
 
+// Token slot -> kernel-facing id, as translate_kv_loc_for_kernel computes it
+// (prhub report on sglang PR #34602, 关键源码片段 multi_ended_allocator.py):
+// page = t / ps, off = t % ps, phys = v2p[page] when a page map is given,
+// id = phys * (ps * 2L) + off, and 0 (the page-0 sink) for a negative slot or
+// a negative phys. A page index past the map or a phys >= P also gives 0 and
+// ORs an error bit into `bits`.
+__device__ __forceinline__ int64_t slot_to_id(const DevPool& p, int64_t t, const int32_t* __restrict__ v2p,
+                                              int64_t v2p_len, int& bits) {
+  if (t < 0) return 0;
+  const int64_t page = div_ps(p, t);
+  const int64_t off = t - page * p.ps;
+  int64_t phys = page;
+  if (v2p != nullptr) {
+    if (page >= v2p_len) {
+      bits |= KV_DEV_ERR_V2P;
+      return 0;
+    }
+    phys = __ldg(v2p + page);
+  }
+  if (phys < 0) return 0;
+  if (phys >= p.num_pages) {
+    bits |= KV_DEV_ERR_ROW;
+    return 0;
+  }
+  return phys * p.stride + off;
+}
+
 // ---- 16-byte loads / stores with explicit cache behaviour ---------------
 
 enum : int {
@@ -155,9 +182,13 @@ __device__ __forceinline__ void copy_rows(const uint4* const (&src)[N], uint4* c
   }
 }
 
-// Cache behaviour of each kernel (measured choices; see the per-kernel notes).
+// Cache behaviour and depth of each kernel: the measured choices on GB300.
+// Gather: block-table pages are often shared by many sequences (common
+// prefixes), so its reads ask L2 to keep lines (evict_last) and its output,
+// which it never re-reads, is streamed (st.cs); on the decode workload this
+// was worth ~2.5% over plain reads, and neutral where pages are read once.
 #ifndef GTKV_GATHER_LD
-#define GTKV_GATHER_LD kLdNc
+#define GTKV_GATHER_LD kLdNcKeep
 #endif
 #ifndef GTKV_GATHER_ST
 #define GTKV_GATHER_ST kStStream
@@ -170,6 +201,13 @@ __device__ __forceinline__ void copy_rows(const uint4* const (&src)[N], uint4* c
 #endif
 #ifndef GTKV_MOVE_ST
 #define GTKV_MOVE_ST kStPlain
+#endif
+// 16-byte vectors each lane keeps in flight (loads issued before stores)
+#ifndef GTKV_STORE_VEC
+#define GTKV_STORE_VEC 16
+#endif
+#ifndef GTKV_MOVE_VEC
+#define GTKV_MOVE_VEC 8
 #endif
 
 // Row geometry chosen on the host from R/16; the list of instantiations.
@@ -227,15 +265,36 @@ inline unsigned grid_for(K kernel, int64_t warps_needed, int sm_count) {
   return static_cast<unsigned>(blocks);
 }
 
+// Tasks per warp batch for the row-task kernels (store, move): lanes hold the
+// metadata of up to 32 tasks, copied in waves of `wave` tasks. Large calls
+// take full 32-task batches; small ones shrink the batch (to a multiple of
+// the wave) so that the work still spreads over every SM.
+template <class K>
+inline int task_batch(K kernel, int64_t n_tasks, int wave, int sm_count) {
+  const int64_t warps_full = static_cast<int64_t>(sm_count) * blocks_per_sm(kernel) * (kBlock / 32);
+  int64_t b = (n_tasks + warps_full - 1) / warps_full;
+  if (wave > 32) wave = 32;
+  b = (b + wave - 1) / wave * wave;
+  if (b < wave) b = wave;
+  if (b > 32) b = 32 / wave * wave;
+  return static_cast<int>(b);
+}
+
 // ---- launchers (one translation unit each) --------------------------------
 
 cudaError_t launch_translate(const DevPool& p, const int64_t* slots, int64_t n, const int32_t* v2p,
                              int64_t v2p_len, int32_t* ids, int sm_count, cudaStream_t s);
 cudaError_t launch_store(const DevPool& p, int32_t layer0, int32_t n_layers, const int32_t* ids, int64_t n,
                          const void* k, const void* v, int sm_count, cudaStream_t s);
+cudaError_t launch_store_slots(const DevPool& p, int32_t layer0, int32_t n_layers, const int64_t* slots, int64_t n,
+                               const int32_t* v2p, int64_t v2p_len, const void* k, const void* v, int sm_count,
+                               cudaStream_t s);
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
                           const int32_t* seq_start, const int32_t* seq_len, const int64_t* cu, void* out_k,
                           void* out_v, int64_t out_rows, int sm_count, cudaStream_t s);
+cudaError_t launch_block_table(const DevPool& p, const int32_t* virt, int32_t n_seqs, int32_t max_pages,
+                               const int32_t* seq_len, const int32_t* v2p, int64_t v2p_len, int32_t* out,
+                               int sm_count, cudaStream_t s);
 cudaError_t launch_move(const DevPool& p, const int32_t* src, const int32_t* dst, int64_t n, int sm_count,
                         cudaStream_t s);
 

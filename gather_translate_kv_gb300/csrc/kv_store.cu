@@ -16,70 +16,121 @@ namespace {
 
 // Tasks t in [0, n_tasks), n_tasks = n_layers * n: layer = layer0 + t / n,
 // token i = t % n; the input rows are K[t] and V[t] (a [n_layers, n, H, D]
-// layout, n_layers = 1 for the per-layer call). A warp takes TPU = (32/G)*U
-// consecutive tasks at a time; lane 0 of each row group reads the id and
-// shares the destination row by shuffle.
-template <int G, int VPL, int U>
+// layout, n_layers = 1 for the per-layer call). A warp takes 32 consecutive
+// tasks at a time: lane k reads the id of task t0 + k (one coalesced load for
+// the batch, issued one batch ahead so its latency hides behind the copies),
+// then the warp copies the batch in waves of 32/G tasks, each task's
+// destination row shared by shuffle from the lane that owns it.
+//
+// With SLOTS the tasks carry token slots instead of ids, and each lane
+// translates its own (translate fused into the store: one launch, no id
+// buffer); a tombstone then lands on the sink exactly as kv_translate's id 0
+// would.
+template <int G, int VPL, int U, bool SLOTS>
 __global__ void __launch_bounds__(kBlock) k_store(DevPool p, int32_t layer0, int64_t n, int64_t n_tasks,
-                                                  const int32_t* __restrict__ ids, const uint4* __restrict__ K,
-                                                  const uint4* __restrict__ V) {
+                                                  const int32_t* __restrict__ ids, const int64_t* __restrict__ slots,
+                                                  const int32_t* __restrict__ v2p, int64_t v2p_len,
+                                                  const uint4* __restrict__ K, const uint4* __restrict__ V,
+                                                  int batch) {
   constexpr int RPW = 32 / G;
-  constexpr int TPU = RPW * U;
   const int lane = threadIdx.x & 31;
   const int g = lane % G;
   const int grp = lane / G;
   const int64_t vpr = VPL > 0 ? static_cast<int64_t>(G) * VPL : p.vpr;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t step = ((static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) * batch;
   const bool one_layer = n_tasks == n;
   const L2Policy pol = make_l2_policy();
 
-  for (int64_t t0 = warp * TPU; t0 < n_tasks; t0 += nwarps * TPU) {
-    const uint4* src[2 * U];
-    uint4* dst[2 * U];
-    bool go[2 * U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t t = t0 + u * RPW + grp;
-      long long row = -1;  // K row of this task, in view units; -1 = skip
-      if (g == 0 && t < n_tasks) {
-        const int64_t l = one_layer ? 0 : t / n;
-        const int32_t id = __ldg(ids + (t - l * n));
-        if (id >= 0 && id < p.n_rows) {
-          row = id + 2 * (layer0 + l) * p.ps;
-        } else {
-          atomicOr(p.err, KV_DEV_ERR_ROW);
-        }
-      }
-      row = __shfl_sync(kFull, row, lane & ~(G - 1));
-      const bool ok = row >= 0;
-      go[2 * u] = go[2 * u + 1] = ok;
-      const int64_t tt = ok ? t : 0;
-      const int64_t rr = ok ? row : 0;
-      src[2 * u] = K + tt * vpr;
-      src[2 * u + 1] = V + tt * vpr;
-      dst[2 * u] = p.base + rr * vpr;
-      dst[2 * u + 1] = p.base + (rr + p.ps) * vpr;
+  int64_t t0 = warp * batch;
+  const bool mine = lane < batch;  // lane owns a task of the batch
+  int64_t l_next = 0;
+  int64_t id_next = -1;
+  int bits = 0;
+  auto fetch = [&](int64_t t) {
+    l_next = (one_layer || t >= n_tasks) ? 0 : t / n;
+    if (t >= n_tasks) {
+      id_next = -1;
+    } else if constexpr (SLOTS) {
+      id_next = __ldg(slots + (t - l_next * n));  // translated below, once the load has landed
+    } else {
+      id_next = __ldg(ids + (t - l_next * n));
     }
-    copy_rows<G, VPL, 2 * U, GTKV_STORE_LD, GTKV_STORE_ST>(src, dst, go, g, vpr, pol);
+  };
+  fetch(mine ? t0 + lane : n_tasks);
+  for (; t0 < n_tasks; t0 += step) {
+    const int64_t t = mine ? t0 + lane : n_tasks;
+    int64_t id = id_next;
+    const int64_t l = l_next;
+    fetch(mine ? t0 + step + lane : n_tasks);  // next batch's ids, in flight during this batch's copies
+    if constexpr (SLOTS) {
+      if (t < n_tasks) id = slot_to_id(p, id, v2p, v2p_len, bits);
+    }
+    long long row = -1;  // K row of this lane's task, in view units; -1 = skip
+    if (t < n_tasks) {
+      if (id >= 0 && id < p.n_rows) {
+        row = id + 2 * (layer0 + l) * p.ps;
+      } else {
+        atomicOr(p.err, KV_DEV_ERR_ROW);
+      }
+    }
+    const int cnt = static_cast<int>(n_tasks - t0 < batch ? n_tasks - t0 : batch);
+#pragma unroll 1
+    for (int w0 = 0; w0 < cnt; w0 += RPW * U) {
+      const uint4* src[2 * U];
+      uint4* dst[2 * U];
+      bool go[2 * U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = w0 + u * RPW + grp;  // task within the batch
+        const long long rr = __shfl_sync(kFull, row, j & 31);
+        const bool ok = j < cnt && rr >= 0;
+        const int64_t tt = ok ? t0 + j : 0;
+        const int64_t r_ = ok ? rr : 0;
+        go[2 * u] = go[2 * u + 1] = ok;
+        src[2 * u] = K + tt * vpr;
+        src[2 * u + 1] = V + tt * vpr;
+        dst[2 * u] = p.base + r_ * vpr;
+        dst[2 * u + 1] = p.base + (r_ + p.ps) * vpr;
+      }
+      copy_rows<G, VPL, 2 * U, GTKV_STORE_LD, GTKV_STORE_ST>(src, dst, go, g, vpr, pol);
+    }
   }
+  if constexpr (SLOTS) {
+    if (bits) atomicOr(p.err, bits);
+  }
+}
+
+template <bool SLOTS>
+cudaError_t launch(const DevPool& p, int32_t layer0, int32_t n_layers, const int32_t* ids, const int64_t* slots,
+                   int64_t n, const int32_t* v2p, int64_t v2p_len, const void* k, const void* v, int sm_count,
+                   cudaStream_t s) {
+  const int64_t n_tasks = n * n_layers;
+  return dispatch_row(p.vpr, [&]<int G, int VPL>() -> cudaError_t {
+    // GTKV_STORE_VEC row vectors in flight per lane (K and V of U tasks)
+    // (U capped at G so that one wave set, (32/G)*U tasks, fits in a 32-task batch)
+    constexpr int U0 = VPL == 0 ? 1 : (2 * VPL >= GTKV_STORE_VEC ? 1 : GTKV_STORE_VEC / (2 * VPL));
+    constexpr int U = U0 < G ? U0 : G;
+    auto kernel = k_store<G, VPL, U, SLOTS>;
+    const int batch = task_batch(kernel, n_tasks, (32 / G) * U, sm_count);
+    const unsigned grid = grid_for(kernel, (n_tasks + batch - 1) / batch, sm_count);
+    kernel<<<grid, kBlock, 0, s>>>(p, layer0, n, n_tasks, ids, slots, v2p, v2p_len, static_cast<const uint4*>(k),
+                                   static_cast<const uint4*>(v), batch);
+    return cudaGetLastError();
+  });
 }
 
 }  // namespace
 
 cudaError_t launch_store(const DevPool& p, int32_t layer0, int32_t n_layers, const int32_t* ids, int64_t n,
                          const void* k, const void* v, int sm_count, cudaStream_t s) {
-  const int64_t n_tasks = n * n_layers;
-  return dispatch_row(p.vpr, [&]<int G, int VPL>() -> cudaError_t {
-    // about 8 row vectors in flight per lane (K and V of U tasks)
-    constexpr int U = VPL == 0 ? 1 : (VPL >= 4 ? 1 : 4 / VPL);
-    auto kernel = k_store<G, VPL, U>;
-    const int64_t tpu = (32 / G) * U;
-    const unsigned grid = grid_for(kernel, (n_tasks + tpu - 1) / tpu, sm_count);
-    kernel<<<grid, kBlock, 0, s>>>(p, layer0, n, n_tasks, ids, static_cast<const uint4*>(k),
-                                   static_cast<const uint4*>(v));
-    return cudaGetLastError();
-  });
+  return launch<false>(p, layer0, n_layers, ids, nullptr, n, nullptr, 0, k, v, sm_count, s);
+}
+
+cudaError_t launch_store_slots(const DevPool& p, int32_t layer0, int32_t n_layers, const int64_t* slots, int64_t n,
+                               const int32_t* v2p, int64_t v2p_len, const void* k, const void* v, int sm_count,
+                               cudaStream_t s) {
+  return launch<true>(p, layer0, n_layers, nullptr, slots, n, v2p, v2p_len, k, v, sm_count, s);
 }
 
 }  // namespace gtkv

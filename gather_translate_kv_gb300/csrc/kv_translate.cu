@@ -16,33 +16,64 @@ __global__ void __launch_bounds__(kBlock) k_translate(DevPool p, const int64_t* 
                                                       int32_t* __restrict__ ids) {
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += step) {
-    const int64_t t = __ldg(slots + i);
-    int64_t id = 0;
-    if (t >= 0) {
-      const int64_t page = div_ps(p, t);
-      const int64_t off = t - page * p.ps;
-      int64_t phys = page;
-      if (v2p != nullptr) {
-        if (page < v2p_len) {
-          phys = __ldg(v2p + page);
-        } else {
-          phys = -1;
-          bits |= KV_DEV_ERR_V2P;
-        }
-      }
-      if (phys >= p.num_pages) {
-        phys = -1;
-        bits |= KV_DEV_ERR_ROW;
-      }
-      if (phys >= 0) id = phys * p.stride + off;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += step)
+    ids[i] = static_cast<int32_t>(slot_to_id(p, __ldg(slots + i), v2p, v2p_len, bits));
+  if (bits) atomicOr(p.err, bits);
+}
+
+// Kernel-facing block table, prefix only: one table entry per thread.
+// Entry k of sequence s is translated when k < ceil(len_s / ps) (capped at
+// max_pages): virtual page -> physical page through the map, scaled by the
+// row-blocks per page (2L) so that entry * ps + offset is the kernel-facing
+// id; tombstones and errors give 0, the sink page. Later entries are untouched.
+// virt and out may be the same buffer (in place): each thread reads its own
+// entry before writing it, so neither pointer is declared __restrict__.
+__global__ void __launch_bounds__(kBlock) k_block_table(DevPool p, const int32_t* virt,
+                                                        int32_t n_seqs, int32_t max_pages,
+                                                        const int32_t* __restrict__ seq_len,
+                                                        const int32_t* __restrict__ v2p, int64_t v2p_len,
+                                                        int32_t* out) {
+  int bits = 0;
+  const int64_t n = static_cast<int64_t>(n_seqs) * max_pages;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += step) {
+    const int64_t s = e / max_pages;
+    const int64_t k = e - s * max_pages;
+    const int64_t len = __ldg(seq_len + s);
+    int64_t np = len > 0 ? div_ps(p, len + p.ps - 1) : 0;
+    if (np > max_pages) {
+      if (k == 0) bits |= KV_DEV_ERR_TABLE;
+      np = max_pages;
     }
-    ids[i] = static_cast<int32_t>(id);
+    if (k >= np) continue;
+    const int64_t vp = virt[e];
+    int64_t phys = -1;
+    if (vp >= 0) {
+      if (vp < v2p_len) {
+        phys = __ldg(v2p + vp);
+      } else {
+        bits |= KV_DEV_ERR_V2P;
+      }
+    }
+    if (phys >= p.num_pages) {
+      bits |= KV_DEV_ERR_ROW;
+      phys = -1;
+    }
+    out[e] = static_cast<int32_t>(phys < 0 ? 0 : phys * p.blocks);
   }
   if (bits) atomicOr(p.err, bits);
 }
 
 }  // namespace
+
+cudaError_t launch_block_table(const DevPool& p, const int32_t* virt, int32_t n_seqs, int32_t max_pages,
+                               const int32_t* seq_len, const int32_t* v2p, int64_t v2p_len, int32_t* out,
+                               int sm_count, cudaStream_t s) {
+  const int64_t warps = (static_cast<int64_t>(n_seqs) * max_pages + 31) / 32;
+  const unsigned grid = grid_for(k_block_table, warps, sm_count);
+  k_block_table<<<grid, kBlock, 0, s>>>(p, virt, n_seqs, max_pages, seq_len, v2p, v2p_len, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_translate(const DevPool& p, const int64_t* slots, int64_t n, const int32_t* v2p,
                              int64_t v2p_len, int32_t* ids, int sm_count, cudaStream_t s) {

@@ -179,6 +179,28 @@ int kv_store_layer(const kv_pool_t* pool, int32_t layer, const int32_t* ids_dev,
 int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n, const void* k_all_dev,
                         const void* v_all_dev, kv_stream_t stream);
 
+/* Fused translate + per-layer store: exactly kv_translate of slots_dev (with
+ * the optional page map) followed by kv_store_layer, in one launch and with
+ * no id buffer: each task translates its own slot.
+ * Source: translate_kv_loc_for_kernel (关键源码片段 multi_ended_allocator.py)
+ * and _store_kv_layer (关键文件 memory_pool.py); the report's related
+ * write-path change (关联脉络, PR #35245) translates the write location once
+ * per forward batch, which this call folds into the store itself.
+ *  slots_dev  int64 [n] token slots (negative = tombstone -> page-0 sink)
+ *  v2p_dev    int32 [v2p_len] virtual -> physical page map, or NULL
+ *  k_dev, v_dev  as kv_store_layer
+ * Device errors: as kv_translate (KV_DEV_ERR_V2P, KV_DEV_ERR_ROW; the token
+ * is then stored to the sink, as kv_translate's id 0 would be). */
+int kv_store_layer_slots(const kv_pool_t* pool, int32_t layer, const int64_t* slots_dev, int64_t n,
+                         const int32_t* v2p_dev, int64_t v2p_len, const void* k_dev, const void* v_dev,
+                         kv_stream_t stream);
+
+/* Fused translate + all-layer store: kv_translate followed by
+ * kv_store_all_layers, in one launch.
+ *  k_all_dev, v_all_dev  [L, n, H, D] contiguous (layer-major), 16-byte aligned */
+int kv_store_all_layers_slots(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int32_t* v2p_dev,
+                              int64_t v2p_len, const void* k_all_dev, const void* v_all_dev, kv_stream_t stream);
+
 /* Block-table gather of one layer into packed K and V outputs.
  * Source: the read path the report describes -- each layer's K/V read
  * "through one contiguous tensor and one shared block table" (功能与动机) --
@@ -219,6 +241,28 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
  * skipped. */
 int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* dst_ids_dev, int64_t n,
             kv_stream_t stream);
+
+/* Kernel-facing block table, prefix only: for each sequence s, the first
+ * ceil(seq_len[s] / ps) entries (at most max_pages) of its virtual page list
+ * are mapped through the virtual -> physical page map and scaled by the
+ * row-blocks per page, out = phys * 2L, so that out * ps + offset is the
+ * token's kernel-facing id (the id kv_translate gives the same virtual slot).
+ * Entries past the prefix are left untouched.
+ * Source: the report's read-path change (关联脉络, PR #35247: the read path's
+ * kernel-facing page table is built once, translating only the prefix a
+ * sequence uses) over translate_kv_loc_for_kernel's page arithmetic
+ * (关键源码片段 multi_ended_allocator.py).
+ *  virt_bt_dev  int32 [n_seqs, max_pages] virtual pages (negative = tombstone)
+ *  seq_len_dev  int32 [n_seqs] tokens per sequence
+ *  v2p_dev      int32 [v2p_len] virtual -> physical page map (negative = tombstone)
+ *  out_bt_dev   int32 [n_seqs, max_pages]; may be virt_bt_dev itself (in place)
+ * A tombstone becomes 0, the sink page (reads of it land in the sink, like a
+ * clamped id). Device errors: a virtual page >= v2p_len sets KV_DEV_ERR_V2P,
+ * a physical page >= num_pages sets KV_DEV_ERR_ROW (both write 0), and
+ * seq_len[s] > max_pages * ps sets KV_DEV_ERR_TABLE (the prefix is capped). */
+int kv_translate_block_table(const kv_pool_t* pool, const int32_t* virt_bt_dev, int32_t n_seqs, int32_t max_pages,
+                             const int32_t* seq_len_dev, const int32_t* v2p_dev, int64_t v2p_len,
+                             int32_t* out_bt_dev, kv_stream_t stream);
 
 /* Read and clear the pool's device error word. Synchronizes `stream`, then
  * writes the KV_DEV_ERR_* bits raised since the last read into *dev_code and

@@ -114,6 +114,8 @@ def lib(path: str | None = None):
         L.ora_gather_rows.restype = ctypes.c_int
         L.ora_move_rows.argtypes = [P(_Desc), vp, vp, c64, vp, vp]
         L.ora_move_rows.restype = ctypes.c_int
+        L.ora_block_table_kf.argtypes = [P(_Desc), vp, c32, c32, vp, vp, c64, vp]
+        L.ora_block_table_kf.restype = ctypes.c_int
         if path is not None:
             return L
         _lib = L
@@ -261,3 +263,15 @@ class Oracle:
         db = np.empty(s.size * nb, np.int64)
         err = self._L.ora_move_rows(ctypes.byref(self._d), _ptr(s), _ptr(d), s.size, _ptr(sb), _ptr(db))
         return sb, db, err
+
+    # kernel-facing block table ---------------------------------------------
+    def block_table_kf(self, virt_bt, seq_len, v2p, out=None):
+        """Prefix-only kernel-facing table: (out int32 [S, maxp], err)."""
+        vb = np.ascontiguousarray(virt_bt, dtype=np.int32)
+        n_seqs, max_pages = vb.shape
+        ln = np.ascontiguousarray(seq_len, dtype=np.int32)
+        v = np.ascontiguousarray(v2p, dtype=np.int32)
+        out = np.full(vb.shape, -7, np.int32) if out is None else np.ascontiguousarray(out, dtype=np.int32)
+        err = self._L.ora_block_table_kf(ctypes.byref(self._d), _ptr(vb), n_seqs, max_pages, _ptr(ln), _ptr(v),
+                                         v.size, _ptr(out))
+        return out, err

@@ -423,3 +423,46 @@ int ora_move_rows(const ora_desc* d, const int32_t* src_ids, const int32_t* dst_
     }
     return err;
 }
+
+/* ------------------------------------------------------- block table build */
+
+/* Kernel-facing block table, prefix only. The report moves read-path
+ * translation into a "prefix-only" kernel-facing page-table build (关联脉络,
+ * PR #35247; 评论区精华). Reading taken: for sequence s only the pages that
+ * hold its tokens [0, len_s) -- the first ceil(len_s / ps) entries, at most
+ * max_pages -- are translated; later entries are left as they are. Each
+ * translated entry is the physical page scaled by the row-blocks per page,
+ * phys * 2L, so that entry * ps + offset is the token's kernel-facing id, the
+ * same id translate_kv_loc_for_kernel gives the slot (关键源码片段
+ * multi_ended_allocator.py). A tombstone (negative virtual page or negative
+ * map entry) becomes 0, the sink page. A virtual page past the map raises
+ * ORA_E_V2P, a physical page >= P raises ORA_E_ROW; both write 0. len_s >
+ * max_pages * ps raises ORA_E_TABLE (the prefix is capped at max_pages). */
+int ora_block_table_kf(const ora_desc* d, const int32_t* virt, int32_t n_seqs, int32_t max_pages,
+                       const int32_t* seq_len, const int32_t* v2p, int64_t v2p_len, int32_t* out) {
+    int64_t ps = d->page_size;
+    int64_t blocks = 2 * (int64_t)d->layer_num;
+    int err = 0;
+    for (int32_t s = 0; s < n_seqs; ++s) {
+        int64_t len = seq_len[s];
+        int64_t np = len > 0 ? (len + ps - 1) / ps : 0;
+        if (np > max_pages) {
+            err |= ORA_E_TABLE;
+            np = max_pages;
+        }
+        for (int64_t k = 0; k < np; ++k) {
+            int64_t vp = virt[(int64_t)s * max_pages + k];
+            int64_t phys = -1;
+            if (vp >= 0) {
+                if (vp >= v2p_len) err |= ORA_E_V2P;
+                else phys = v2p[vp];
+            }
+            if (phys >= d->num_pages) {
+                err |= ORA_E_ROW;
+                phys = -1;
+            }
+            out[(int64_t)s * max_pages + k] = (int32_t)(phys < 0 ? 0 : phys * blocks);
+        }
+    }
+    return err;
+}

@@ -351,9 +351,40 @@ def pin_address_mode(so):
         assert np.array_equal(M[b:b + R], before[a:a + R])
 
 
+def pin_block_table_kf(so):
+    """Prefix-only kernel-facing block table: hand-computed entries
+    (tests/golden/block_table_tiny.txt), untouched entries past each prefix,
+    and every entry*ps + o equal to translate's id of the same virtual slot."""
+    o = _mk(so, _geom(2, 2, 8, 2, 4, 64))
+    v2p = np.arange(41, dtype=np.int32) + 10
+    v2p[7] = -1
+    v2p[9] = 70
+    rows = [r for r in _rows(os.path.join(GOLDEN, "block_table_tiny.txt"))]
+    ln = np.array([int(r[0]) for r in rows], np.int32)
+    virt = np.array([[int(x) for x in r[2:7]] for r in rows], np.int32)
+    want = np.array([[int(x) for x in r[8:13]] for r in rows], np.int32)
+    got, err = o.block_table_kf(virt, ln, v2p)
+    assert err == 0 and np.array_equal(got, want), got
+    for s_ in range(len(rows)):
+        np_ = -(-int(ln[s_]) // 4)
+        for k in range(np_):
+            for off in range(4):
+                slot = int(virt[s_, k]) * 4 + off
+                ids, _ = o.translate(np.array([slot], np.int64), v2p)
+                assert int(ids[0]) == (int(got[s_, k]) * 4 + off if got[s_, k] else int(ids[0]))
+                if got[s_, k]:
+                    assert int(ids[0]) == int(got[s_, k]) * 4 + off
+    # errors: a virtual page past the map, a physical page past the pool, an overlong sequence
+    bad, err = o.block_table_kf(np.array([[41, 9, 1]], np.int32), np.array([12], np.int32), v2p)
+    assert err == oracle.E_V2P | oracle.E_ROW and list(bad[0]) == [0, 0, 44]
+    _, err = o.block_table_kf(np.array([[1, 2]], np.int32), np.array([9], np.int32), v2p)
+    assert err == oracle.E_TABLE
+
+
 PINS = [
     pin_translate_golden, pin_layout_table, pin_gates, pin_bijection, pin_store_vs_strided,
     pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors, pin_address_mode,
+    pin_block_table_kf,
 ]
 
 

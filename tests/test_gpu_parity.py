@@ -252,8 +252,9 @@ def test_error_paths_match_oracle():
         assert err == oracle.E_ROW | oracle.E_TABLE
         assert pp.last_error() == dev_bits(err)
         # rows the oracle writes and the kernel writes agree wherever the
-        # metadata is consistent (sequences 0 and 2)
-        for r0, r1 in ((0, 16), (27, min(rows, 36))):
+        # metadata is consistent: sequence 0 and the rows of sequence 2 that
+        # sequence 1's overlong span does not also cover (those race)
+        for r0, r1 in ((0, 16), (30, min(rows, 36))):
             assert_bytes_equal(dk.cpu().numpy()[r0:r1], ok[r0:r1], "gather K", R)
             assert_bytes_equal(dv.cpu().numpy()[r0:r1], ov[r0:r1], "gather V", R)
     # host-side argument errors
@@ -329,4 +330,96 @@ def test_calls_capture_in_a_cuda_graph():
         assert_bytes_equal(ov_d.cpu().numpy(), rv, "graph gather V", R)
         assert_pool_matches(pp, M0, {})
     assert pp.last_error() == 0
+    pp.close()
+
+
+@pytest.mark.parametrize("shape,anchor", SHAPES[:6], ids=IDS[:6])
+def test_fused_translate_store_matches_oracle(shape, anchor):
+    """kv_store_layer_slots / kv_store_all_layers_slots (translate fused into
+    the store) against the oracle's store, which takes slots natively; with a
+    page map that tombstones some pages, and with a map too short (errors)."""
+    rng = np.random.default_rng(300 + shape.row_bytes + shape.page_size)
+    pp = PoolPair(shape, anchor)
+    o, R, L = pp.o, pp.R, shape.layer_num
+    ps, P = shape.page_size, shape.num_pages
+    M0 = pp.M.copy()
+    hi = _store_pages(shape)
+    v2p = np.arange(P, dtype=np.int32)
+    v2p[1:hi] = (1 + rng.permutation(hi - 1)).astype(np.int32)  # virtual pages 1..hi-1 shuffled
+    v2p[rng.choice(np.arange(1, hi), size=max(1, hi // 6), replace=False)] = -1
+    tombs: dict = {}
+    for layer in sorted({0, L - 1}):
+        slots = _tokens(shape, rng, 257, 6)
+        K, V = _vals(shape, rng, (slots.size,))
+        err = o.store(pp.M, layer, slots, K, V, v2p)
+        gt.kv_store_layer_slots(pp.pool, layer, to_dev(slots), to_dev(K), to_dev(V), to_dev(v2p))
+        assert pp.last_error() == dev_bits(err) == 0
+        # tombstoned slots and slots on tombstoned pages both land on the sink
+        sunk = (slots < 0) | (v2p[np.maximum(slots, 0) // ps] < 0)
+        tombs = merge(tombs, tomb_inputs(np.where(sunk, -1, slots), K, V, layer, R))
+        assert_pool_matches(pp, M0, tombs)
+    slots = _tokens(shape, rng, 190, 3)
+    Ka, Va = _vals(shape, rng, (L, slots.size))
+    err = o.store_all(pp.M, slots, Ka, Va, v2p)
+    gt.kv_store_all_layers_slots(pp.pool, to_dev(slots), to_dev(Ka), to_dev(Va), to_dev(v2p))
+    assert pp.last_error() == dev_bits(err) == 0
+    sunk = (slots < 0) | (v2p[np.maximum(slots, 0) // ps] < 0)
+    for layer in range(L):
+        tombs = merge(tombs, tomb_inputs(np.where(sunk, -1, slots), Ka[layer], Va[layer], layer, R))
+    assert_pool_matches(pp, M0, tombs)
+    # a page map shorter than the pages used: those tokens go to the sink with V2P set
+    short = v2p[: max(2, hi // 2)].copy()
+    slots = _tokens(shape, rng, 100, 0)
+    K, V = _vals(shape, rng, (slots.size,))
+    err = o.store(pp.M, 0, slots, K, V, short)
+    gt.kv_store_layer_slots(pp.pool, 0, to_dev(slots), to_dev(K), to_dev(V), to_dev(short))
+    assert err & oracle.E_V2P and pp.last_error() == dev_bits(err)
+    vp_ = np.maximum(slots, 0) // ps
+    sunk = (slots < 0) | (vp_ >= short.size) | (short[np.minimum(vp_, short.size - 1)] < 0)
+    tombs = merge(tombs, tomb_inputs(np.where(sunk, -1, slots), K, V, 0, R))
+    assert_pool_matches(pp, M0, tombs)
+    pp.close()
+
+
+@pytest.mark.parametrize("shape", [synth.SHAPES[1], synth.SHAPES[2].scaled(300), synth.SHAPES[5].scaled(64),
+                                   S(0, "odd", 3, 1, 16, 1, 3, 90)], ids=lambda s: s.name)
+def test_block_table_matches_oracle(shape):
+    """kv_translate_block_table against the oracle (entries, untouched tails,
+    error bits), in place and out of place, and entry*ps + o equal to
+    kv_translate's id of the same virtual slot."""
+    rng = np.random.default_rng(400 + shape.page_size)
+    pp = PoolPair(shape, mirror=False)
+    ps, P = shape.page_size, shape.num_pages
+    S_, maxp = 37, 9
+    V = P + 5  # virtual page space, a few past the physical pages
+    v2p = rng.permutation(V).astype(np.int32) % P
+    v2p[rng.choice(V, size=V // 8, replace=False)] = -1
+    virt = rng.integers(-1, V, size=(S_, maxp)).astype(np.int32)
+    ln = rng.integers(0, maxp * ps + 1, size=S_).astype(np.int32)
+    want, err = pp.o.block_table_kf(virt, ln, v2p, out=np.full(virt.shape, -7, np.int32))
+    assert err == 0
+    out = torch.full(virt.shape, -7, dtype=torch.int32, device="cuda")
+    gt.kv_translate_block_table(pp.pool, to_dev(virt), to_dev(ln), to_dev(v2p), out)
+    assert pp.last_error() == 0
+    assert np.array_equal(out.cpu().numpy(), want)
+    # in place; a short map and an overlong sequence raise their bits
+    short = v2p[: V // 2].copy()
+    ln2 = ln.copy()
+    ln2[3] = maxp * ps + 2
+    pre = np.where(np.arange(maxp)[None, :] < -(-ln2[:, None] // ps), virt, -7).astype(np.int32)
+    want2, err2 = pp.o.block_table_kf(virt, ln2, short, out=pre.copy())
+    vt = to_dev(pre.copy())
+    vt.copy_(to_dev(virt))
+    gt.kv_translate_block_table(pp.pool, vt, to_dev(ln2), to_dev(short))  # out_bt = virt_bt
+    assert pp.last_error() == dev_bits(err2) and err2 & oracle.E_TABLE
+    got2 = vt.cpu().numpy()
+    mask = np.arange(maxp)[None, :] < np.minimum(-(-ln2[:, None] // ps), maxp)
+    assert np.array_equal(got2[mask], want2[mask]) and np.array_equal(got2[~mask], virt[~mask])
+    # consistency with kv_translate on the same virtual slots
+    kk = np.nonzero(mask & (want > 0))
+    offs = rng.integers(0, ps, size=kk[0].size)
+    slots = virt[kk].astype(np.int64) * ps + offs
+    ids = torch.empty(slots.size, dtype=torch.int32, device="cuda")
+    gt.kv_translate(pp.pool, to_dev(slots), ids, to_dev(v2p))
+    assert np.array_equal(ids.cpu().numpy(), want[kk].astype(np.int64) * ps + offs)
     pp.close()

@@ -66,6 +66,12 @@ MUTANTS = [
     ("layer_stride_one_block",
      "int64_t page_bytes = (int64_t)d->page_size * blocks * R;",
      "int64_t page_bytes = (int64_t)d->page_size * (blocks - 1) * R;"),
+    ("block_table_entry_not_scaled",
+     "out[(int64_t)s * max_pages + k] = (int32_t)(phys < 0 ? 0 : phys * blocks);",
+     "out[(int64_t)s * max_pages + k] = (int32_t)(phys < 0 ? 0 : phys);"),
+    ("block_table_prefix_floor",
+     "int64_t np = len > 0 ? (len + ps - 1) / ps : 0;",
+     "int64_t np = len > 0 ? len / ps : 0;"),
     ("asymmetric_not_rejected",
      "if (d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;",
      ""),
