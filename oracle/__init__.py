@@ -50,6 +50,8 @@ class _Desc(ctypes.Structure):
         ("page_size", ctypes.c_int32),
         ("num_pages", ctypes.c_int64),
         ("anchor", ctypes.c_int64),
+        ("latent_only", ctypes.c_int32),
+        ("reserved_", ctypes.c_int32),
     ]
 
 
@@ -65,6 +67,11 @@ class Geometry:
     num_pages: int
     anchor: int = 0
     v_head_dim: int | None = None
+    latent_only: bool = False  # MLA: one latent row per layer per token, no V
+
+    @property
+    def blocks(self) -> int:
+        return self.layer_num if self.latent_only else 2 * self.layer_num
 
     def desc(self) -> _Desc:
         return _Desc(
@@ -76,6 +83,8 @@ class Geometry:
             self.page_size,
             self.num_pages,
             self.anchor,
+            1 if self.latent_only else 0,
+            0,
         )
 
 
@@ -177,9 +186,10 @@ class Oracle:
         assert M.dtype == np.uint8 and M.size >= self.raw_bytes()
         slots = np.ascontiguousarray(slots, dtype=np.int64)
         Kb = np.ascontiguousarray(K).view(np.uint8)
-        Vb = np.ascontiguousarray(V).view(np.uint8)
+        Vb = None if V is None else np.ascontiguousarray(V).view(np.uint8)
         R = self.sizes()["row_bytes"]
-        assert Kb.size == slots.size * R and Vb.size == slots.size * R
+        assert Kb.size == slots.size * R and (Vb is None or Vb.size == slots.size * R)
+        assert Vb is not None or self.geom.latent_only
         v = None if v2p is None else np.ascontiguousarray(v2p, dtype=np.int32)
         return self._L.ora_store(
             ctypes.byref(self._d), _ptr(M), int(layer), _ptr(slots), slots.size,
@@ -190,9 +200,10 @@ class Oracle:
         assert M.dtype == np.uint8 and M.size >= self.raw_bytes()
         slots = np.ascontiguousarray(slots, dtype=np.int64)
         Kb = np.ascontiguousarray(K_all).view(np.uint8)
-        Vb = np.ascontiguousarray(V_all).view(np.uint8)
+        Vb = None if V_all is None else np.ascontiguousarray(V_all).view(np.uint8)
         R = self.sizes()["row_bytes"]
         assert Kb.size == self.geom.layer_num * slots.size * R
+        assert Vb is not None or self.geom.latent_only
         v = None if v2p is None else np.ascontiguousarray(v2p, dtype=np.int32)
         return self._L.ora_store_all(
             ctypes.byref(self._d), _ptr(M), _ptr(slots), slots.size,
@@ -213,7 +224,7 @@ class Oracle:
             out_rows = int(cu[-1]) if n_seqs > 0 else 0
         if outK is None:
             outK = np.zeros((out_rows, R), dtype=np.uint8)
-        if outV is None:
+        if outV is None and not self.geom.latent_only:
             outV = np.zeros((out_rows, R), dtype=np.uint8)
         err = self._L.ora_gather(
             ctypes.byref(self._d), _ptr(M), int(layer), _ptr(bt), n_seqs, max_pages,

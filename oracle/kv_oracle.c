@@ -70,7 +70,21 @@ typedef struct {
     int32_t page_size;   /* ps, tokens per page                 */
     int64_t num_pages;   /* P                                   */
     int64_t anchor;      /* byte offset of this sub-pool in raw */
+    int32_t latent_only; /* 0: MHA/SWA, K and V rows per layer  */
+                         /* 1: MLA, one latent row per layer    */
+    int32_t reserved_;
 } ora_desc;
+
+/* Row-blocks per page and the K block of a layer. MHA/SWA pages hold 2L
+ * blocks, K of layer l in block 2l and V in 2l+1 (实现拆解 step 1); MLA
+ * pages hold L blocks, layer l's latent row in block l (实现拆解 step 2:
+ * blocks_per_page() returns 2 * layer_num for MHA and layer_num for MLA). */
+static int64_t blocks_of(const ora_desc* d) {
+    return d->latent_only ? (int64_t)d->layer_num : 2 * (int64_t)d->layer_num;
+}
+static int64_t k_block(const ora_desc* d, int64_t layer) {
+    return d->latent_only ? layer : 2 * layer;
+}
 
 /* ---------------------------------------------------------------- sizes */
 
@@ -82,17 +96,19 @@ typedef struct {
  * assert message says.
  *
  *   out[0] R          = H * D * itemsize           (row_bytes)
- *   out[1] E          = 2L * R                     (entry_bytes)
- *   out[2] page_bytes = ps * 2L * R
+ *   out[1] E          = B * R                      (entry_bytes)
+ *   out[2] page_bytes = ps * B * R
  *   out[3] total      = P * page_bytes             (one sub-pool per pool)
  *   out[4] tail_pad   = ps * E
- *   out[5] n_rows     = P * 2L * ps                (kernel-facing rows)
- *   out[6] last_view_end = anchor + (2L-1)*ps*R + n_rows*R
+ *   out[5] n_rows     = P * B * ps                 (kernel-facing rows)
+ *   out[6] last_view_end = anchor + (B-1)*ps*R + n_rows*R
+ * with B = 2L row-blocks per page for MHA/SWA and B = L for MLA (the MLA
+ * views reach past the last envelope the same way, so the same one-envelope
+ * tail pad is read for them).
  */
 void ora_sizes(const ora_desc* d, int64_t out[7]) {
-    int64_t L = d->layer_num;
     int64_t R = (int64_t)d->head_num * d->head_dim * d->itemsize;
-    int64_t blocks = 2 * L;
+    int64_t blocks = blocks_of(d);
     int64_t page_bytes = (int64_t)d->page_size * blocks * R;
     int64_t n_rows = d->num_pages * blocks * d->page_size;
     out[0] = R;
@@ -116,13 +132,14 @@ int ora_check_desc(const ora_desc* d, int64_t raw_bytes) {
     if (d->layer_num < 1 || d->head_num < 1 || d->head_dim < 1 ||
         d->itemsize < 1 || d->page_size < 1 || d->num_pages < 1 || d->anchor < 0)
         return ORA_BAD_ARG;
-    if (d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;
+    /* unified_memory_supported_for_model: use_mla_backend or not has_asymmetric_kv */
+    if (!d->latent_only && d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;
     if (d->anchor % d->itemsize != 0) return ORA_ANCHOR;
     /* rows = P * 2L * ps, compared against 2^31 without overflowing: every
      * factor is positive, so test by successive division. */
     {
         int64_t limit = ((int64_t)1 << 31) - 1;
-        int64_t blocks = 2 * (int64_t)d->layer_num;
+        int64_t blocks = blocks_of(d);
         if (d->num_pages > limit / blocks) return ORA_ID_BOUND;
         if (d->num_pages * blocks > limit / d->page_size) return ORA_ID_BOUND;
     }
@@ -180,11 +197,12 @@ static int locate_slot(const ora_desc* d, int64_t t, const int32_t* v2p,
 /* Token slots -> kernel-facing int32 ids (translate_kv_loc_for_kernel):
  *     id = phys * (ps * 2L) + t % ps, clamped to 0 for tombstones.
  * This is the report's closed form kernel_id(t) written out as stated, with
- * kernel_page_multiplier fixed to blocks_per_page() = 2L (实现拆解 step 3). */
+ * kernel_page_multiplier fixed to blocks_per_page() = 2L, or L for MLA
+ * (实现拆解 step 3). */
 int ora_translate(const ora_desc* d, const int64_t* slots, int64_t n,
                   const int32_t* v2p, int64_t v2p_len, int32_t* ids) {
     int err = 0;
-    int64_t stride = (int64_t)d->page_size * (2 * (int64_t)d->layer_num);
+    int64_t stride = (int64_t)d->page_size * blocks_of(d);
     for (int64_t i = 0; i < n; ++i) {
         int64_t p, o;
         int sink;
@@ -215,9 +233,12 @@ int64_t ora_slot_row_byte(const ora_desc* d, int64_t slot, const int32_t* v2p,
  * Rows are written in input order; several tombstones all land on the sink
  * rows (page 0, offset 0), the last one written stays.
  *
+ * MLA pools store one latent row per token (K only, block l); V is unused.
+ *
  * With M == NULL nothing is copied: the pass records, for every row i, the
- * byte offsets it would write (kdst[i], vdst[i]); tests use this to check a
- * full-size run without a host mirror of the pool. */
+ * byte offsets it would write (kdst[i], vdst[i], -1 for MLA's absent V);
+ * tests use this to check a full-size run without a host mirror of the
+ * pool. */
 static int store_pass(const ora_desc* d, uint8_t* M, int32_t layer, const int64_t* slots,
                       int64_t n, const int32_t* v2p, int64_t v2p_len,
                       const uint8_t* K, const uint8_t* V, int64_t* kdst, int64_t* vdst) {
@@ -230,11 +251,11 @@ static int store_pass(const ora_desc* d, uint8_t* M, int32_t layer, const int64_
         int64_t p, o;
         int sink;
         err |= locate_slot(d, slots[i], v2p, v2p_len, &p, &o, &sink);
-        int64_t kb = env_byte(d, p, 2 * (int64_t)layer, o);
-        int64_t vb = env_byte(d, p, 2 * (int64_t)layer + 1, o);
+        int64_t kb = env_byte(d, p, k_block(d, layer), o);
+        int64_t vb = d->latent_only ? -1 : env_byte(d, p, k_block(d, layer) + 1, o);
         if (M != NULL) {
             memcpy(M + kb, K + i * R, (size_t)R);
-            memcpy(M + vb, V + i * R, (size_t)R);
+            if (vb >= 0) memcpy(M + vb, V + i * R, (size_t)R);
         } else {
             kdst[i] = kb;
             vdst[i] = vb;
@@ -266,7 +287,7 @@ int ora_store_all(const ora_desc* d, uint8_t* M, const int64_t* slots, int64_t n
     int err = 0;
     for (int32_t l = 0; l < d->layer_num; ++l)
         err |= ora_store(d, M, l, slots, n, v2p, v2p_len,
-                         K_all + (int64_t)l * n * R, V_all + (int64_t)l * n * R);
+                         K_all + (int64_t)l * n * R, V_all ? V_all + (int64_t)l * n * R : NULL);
     return err;
 }
 
@@ -314,11 +335,11 @@ static int gather_pass(const ora_desc* d, const uint8_t* M, int32_t layer,
             if (p >= d->num_pages) { err |= ORA_E_ROW; continue; }
             int64_t r = cu[s] + (j - st);
             if (r < 0 || r >= out_rows) continue;
-            int64_t kb = env_byte(d, p, 2 * (int64_t)layer, o);
-            int64_t vb = env_byte(d, p, 2 * (int64_t)layer + 1, o);
+            int64_t kb = env_byte(d, p, k_block(d, layer), o);
+            int64_t vb = d->latent_only ? -1 : env_byte(d, p, k_block(d, layer) + 1, o);
             if (M != NULL) {
                 memcpy(outK + r * R, M + kb, (size_t)R);
-                memcpy(outV + r * R, M + vb, (size_t)R);
+                if (vb >= 0) memcpy(outV + r * R, M + vb, (size_t)R);
             } else {
                 ksrc[r] = kb;
                 vsrc[r] = vb;
@@ -351,7 +372,7 @@ int ora_gather_rows(const ora_desc* d, int32_t layer, const int32_t* bt, int32_t
 /* Decode a kernel-facing id into (page, offset): p = id / (ps*2L),
  * o = id % (ps*2L), which must be < ps for an id that translate can produce. */
 static int decode_id(const ora_desc* d, int64_t id, int64_t* p, int64_t* o) {
-    int64_t stride = (int64_t)d->page_size * (2 * (int64_t)d->layer_num);
+    int64_t stride = (int64_t)d->page_size * blocks_of(d);
     int64_t n_rows = d->num_pages * stride;
     if (id < 0 || id >= n_rows) return ORA_E_ROW;
     *p = id / stride;
@@ -370,7 +391,7 @@ int ora_move(const ora_desc* d, uint8_t* M, const int32_t* src_ids,
     int64_t s7[7];
     ora_sizes(d, s7);
     int64_t R = s7[0];
-    int64_t blocks = 2 * (int64_t)d->layer_num;
+    int64_t blocks = blocks_of(d);
     int err = 0;
     if (m <= 0) return 0;
     uint8_t* snap = (uint8_t*)malloc((size_t)(m * blocks * R));
@@ -410,7 +431,7 @@ int64_t ora_id_row_byte(const ora_desc* d, int64_t id, int32_t block) {
  * -1 for a skipped pair. Returns the same error bits as ora_move. */
 int ora_move_rows(const ora_desc* d, const int32_t* src_ids, const int32_t* dst_ids,
                   int64_t m, int64_t* src_bytes, int64_t* dst_bytes) {
-    int64_t blocks = 2 * (int64_t)d->layer_num;
+    int64_t blocks = blocks_of(d);
     int err = 0;
     for (int64_t i = 0; i < m; ++i) {
         int64_t ps_ = 0, os_ = 0, pd_ = 0, od_ = 0;
@@ -441,7 +462,7 @@ int ora_move_rows(const ora_desc* d, const int32_t* src_ids, const int32_t* dst_
 int ora_block_table_kf(const ora_desc* d, const int32_t* virt, int32_t n_seqs, int32_t max_pages,
                        const int32_t* seq_len, const int32_t* v2p, int64_t v2p_len, int32_t* out) {
     int64_t ps = d->page_size;
-    int64_t blocks = 2 * (int64_t)d->layer_num;
+    int64_t blocks = blocks_of(d);
     int err = 0;
     for (int32_t s = 0; s < n_seqs; ++s) {
         int64_t len = seq_len[s];

@@ -47,8 +47,8 @@ def _rows(path):
     return out
 
 
-def _geom(L, H, D, it, ps, P, anchor=0, Dv=None):
-    return oracle.Geometry(L, H, D, it, ps, P, anchor, Dv)
+def _geom(L, H, D, it, ps, P, anchor=0, Dv=None, latent=False):
+    return oracle.Geometry(L, H, D, it, ps, P, anchor, Dv, latent)
 
 
 def _mk(so, g):
@@ -381,10 +381,75 @@ def pin_block_table_kf(so):
     assert err == oracle.E_TABLE
 
 
+def pin_mla(so):
+    """MLA pools (one latent row per layer, blocks_per_page = L): hand-computed
+    layout and ids (tests/golden/mla_tiny.txt), the id bound, the uniform-row
+    gate not applying, a brute-force bijection, and store / gather / move
+    against the [P, L, ps, H, D] reference."""
+    g = {k: int(v) for k, v in _rows(os.path.join(GOLDEN, "mla_tiny.txt"))}
+    o = _mk(so, _geom(2, 1, 16, 2, 4, 64, latent=True))
+    sz = o.sizes()
+    assert (sz["row_bytes"], sz["page_bytes"], sz["total"], sz["tail_pad"], sz["n_rows"], sz["last_view_end"]) == \
+        (g["row_bytes"], g["page_bytes"], g["total"], g["tail_pad"], g["n_rows"], g["last_view_end"])
+    for t in (0, 5, 255, -1):
+        ids, err = o.translate(np.array([t], np.int64))
+        assert err == 0 and int(ids[0]) == g[f"id_{t}"], (t, int(ids[0]))
+    big = _mk(so, _geom(61, 1, 576, 2, 64, 1000, latent=True)).sizes()
+    assert (big["page_bytes"], big["n_rows"], big["last_view_end"]) == \
+        (g["big_page_bytes"], g["big_n_rows"], g["big_last_view_end"])
+    assert _mk(so, _geom(61, 1, 576, 2, 64, g["big_max_pages_ok"], latent=True)).check() == "ok"
+    assert _mk(so, _geom(61, 1, 576, 2, 64, g["big_max_pages_ok"] + 1, latent=True)).check() == "id_bound"
+    # MLA has no V: the report admits it whatever v_head_dim says
+    assert _mk(so, _geom(2, 1, 16, 2, 4, 64, Dv=128, latent=True)).check() == "ok"
+    # bijection on a tiny MLA pool
+    L, ps, P = 3, 4, 5
+    t_ = _mk(so, _geom(L, 1, 16, 1, ps, P, anchor=32, latent=True))
+    R = t_.sizes()["row_bytes"]
+    ids, _ = t_.translate(np.arange(P * ps, dtype=np.int64))
+    seen = sorted(t_.slot_row_byte(int(t), b) for t in range(P * ps) for b in range(L))
+    assert seen == [32 + R * k for k in range(P * L * ps)]
+    for t, kid in zip(range(P * ps), ids):
+        assert t_.slot_row_byte(t, 1) == 32 + (int(kid) + 1 * ps) * R
+    # store / gather / move against the reference
+    rng = np.random.default_rng(17)
+    L, H, D, it, ps, P = 4, 1, 32, 2, 8, 9
+    o = _mk(so, _geom(L, H, D, it, ps, P, latent=True))
+    M = _fresh(o)
+    T = M.copy()
+    env = strided_ref.envelope(T, L, H, D, it, ps, P, latent=True)
+    for layer in range(L):
+        slots = rng.permutation(np.arange(ps, P * ps))[:30].astype(np.int64)
+        slots[3] = -1
+        K = synth.kv_values(rng, (30, H, D), it)
+        assert o.store(M, layer, slots, K, None) == 0
+        strided_ref.store(env, layer, slots, K, None, latent=True)
+        assert np.array_equal(M, T)
+    Ka = synth.kv_values(rng, (L, 20, H, D), it)
+    slots = rng.permutation(np.arange(ps, P * ps))[:20].astype(np.int64)
+    assert o.store_all(M, slots, Ka, None) == 0
+    for layer in range(L):
+        strided_ref.store(env, layer, slots, Ka[layer], None, latent=True)
+    assert np.array_equal(M, T)
+    bt = rng.integers(1, P, size=(3, 4)).astype(np.int32)
+    gb = synth.GatherBatch(bt, np.array([0, 3, 9], np.int32), np.array([32, 20, 12], np.int32))
+    for layer in range(L):
+        k, v, err = o.gather(M, layer, bt, gb.seq_len, gb.cu, gb.seq_start)
+        rk, _ = strided_ref.gather(env, layer, bt, gb.seq_start, gb.seq_len, latent=True)
+        assert err == 0 and v is None
+        assert np.array_equal(k, rk.reshape(len(rk), -1).view(np.uint8).reshape(k.shape))
+    src = slots[:6]
+    dst = np.setdiff1d(np.arange(ps, P * ps), slots)[:6]
+    si, _ = o.translate(src)
+    di, _ = o.translate(dst)
+    assert o.move(M, si, di) == 0
+    strided_ref.move(env, src, dst)
+    assert np.array_equal(M, T)
+
+
 PINS = [
     pin_translate_golden, pin_layout_table, pin_gates, pin_bijection, pin_store_vs_strided,
     pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors, pin_address_mode,
-    pin_block_table_kf,
+    pin_block_table_kf, pin_mla,
 ]
 
 

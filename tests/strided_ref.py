@@ -20,11 +20,14 @@ import numpy as np
 _DT = {1: np.uint8, 2: np.uint16, 4: np.uint32}
 
 
-def envelope(buf: np.ndarray, L, H, D, itemsize, ps, P, anchor=0) -> np.ndarray:
-    """View of the pool region of ``buf`` (uint8) as [P, 2L, ps, H, D]."""
+def envelope(buf: np.ndarray, L, H, D, itemsize, ps, P, anchor=0, latent=False) -> np.ndarray:
+    """View of the pool region of ``buf`` (uint8) as [P, 2L, ps, H, D], or as
+    [P, L, ps, H, D] for an MLA pool (one latent block per layer, 实现拆解
+    step 2: blocks_per_page() = layer_num for MLA)."""
     R = H * D * itemsize
-    region = buf[anchor : anchor + P * 2 * L * ps * R]
-    return region.view(_DT[itemsize]).reshape(P, 2 * L, ps, H, D)
+    B = L if latent else 2 * L
+    region = buf[anchor : anchor + P * B * ps * R]
+    return region.view(_DT[itemsize]).reshape(P, B, ps, H, D)
 
 
 def _where(t, ps, v2p):
@@ -41,21 +44,27 @@ def _where(t, ps, v2p):
     return page, off
 
 
-def store(env, layer, slots, K, V, v2p=None):
-    """K[i] -> env[page, 2*layer, off], V[i] -> env[page, 2*layer+1, off]."""
+def store(env, layer, slots, K, V, v2p=None, latent=False):
+    """K[i] -> env[page, 2*layer, off], V[i] -> env[page, 2*layer+1, off];
+    for an MLA pool the latent row K[i] -> env[page, layer, off]."""
     P, B, ps, H, D = env.shape
     Kd = np.asarray(K).reshape(-1, H, D)
-    Vd = np.asarray(V).reshape(-1, H, D)
+    Vd = None if latent else np.asarray(V).reshape(-1, H, D)
     for i, t in enumerate(np.asarray(slots)):
         p, o = _where(t, ps, v2p)
-        env[p, 2 * layer, o] = Kd[i]
-        env[p, 2 * layer + 1, o] = Vd[i]
+        if latent:
+            env[p, layer, o] = Kd[i]
+        else:
+            env[p, 2 * layer, o] = Kd[i]
+            env[p, 2 * layer + 1, o] = Vd[i]
 
 
-def gather(env, layer, block_table, seq_start, seq_len):
+def gather(env, layer, block_table, seq_start, seq_len, latent=False):
     """Rows of layer ``layer`` for every sequence's tokens [start, len), in
-    (sequence, token) order; a negative page reads the sink (0, 0)."""
+    (sequence, token) order; a negative page reads the sink (0, 0). For an
+    MLA pool the V list is empty."""
     P, B, ps, H, D = env.shape
+    kb = layer if latent else 2 * layer
     ks, vs = [], []
     for s in range(block_table.shape[0]):
         for j in range(int(seq_start[s]), int(seq_len[s])):
@@ -63,12 +72,11 @@ def gather(env, layer, block_table, seq_start, seq_len):
             off = j % ps
             if page < 0:
                 page, off = 0, 0
-            ks.append(env[page, 2 * layer, off].copy())
-            vs.append(env[page, 2 * layer + 1, off].copy())
-    if not ks:
-        z = np.zeros((0, H, D), env.dtype)
-        return z, z
-    return np.stack(ks), np.stack(vs)
+            ks.append(env[page, kb, off].copy())
+            if not latent:
+                vs.append(env[page, kb + 1, off].copy())
+    z = np.zeros((0, H, D), env.dtype)
+    return (np.stack(ks) if ks else z), (np.stack(vs) if vs else z)
 
 
 def move(env, src_slots, dst_slots):

@@ -25,8 +25,20 @@ def test_pin_holds(pin, oracle_lib):
 # (name, original text, planted mistake)
 MUTANTS = [
     ("stride_drops_factor_2",
-     "int64_t stride = (int64_t)d->page_size * (2 * (int64_t)d->layer_num);\n    for",
-     "int64_t stride = (int64_t)d->page_size * ((int64_t)d->layer_num);\n    for"),
+     "int64_t stride = (int64_t)d->page_size * blocks_of(d);\n    for",
+     "int64_t stride = (int64_t)d->page_size * (int64_t)d->layer_num;\n    for"),
+    ("mha_blocks_per_page_L",
+     "return d->latent_only ? (int64_t)d->layer_num : 2 * (int64_t)d->layer_num;",
+     "return d->latent_only ? (int64_t)d->layer_num : (int64_t)d->layer_num;"),
+    ("mla_blocks_per_page_2L",
+     "return d->latent_only ? (int64_t)d->layer_num : 2 * (int64_t)d->layer_num;",
+     "return 2 * (int64_t)d->layer_num;"),
+    ("mla_latent_in_block_2l",
+     "return d->latent_only ? layer : 2 * layer;",
+     "return 2 * layer;"),
+    ("mla_asymmetric_rejected",
+     "if (!d->latent_only && d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;",
+     "if (d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;"),
     ("tail_pad_one_block_short",
      "out[4] = (int64_t)d->page_size * (blocks * R);",
      "out[4] = (int64_t)d->page_size * ((blocks - 1) * R);"),
@@ -73,7 +85,7 @@ MUTANTS = [
      "int64_t np = len > 0 ? (len + ps - 1) / ps : 0;",
      "int64_t np = len > 0 ? len / ps : 0;"),
     ("asymmetric_not_rejected",
-     "if (d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;",
+     "if (!d->latent_only && d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;",
      ""),
 ]
 
