@@ -188,49 +188,86 @@ def profiled_traffic(summary="gather_decode_llama3_8b.txt", sources=GATHER_SOURC
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(budget_s: float = 12.0):
-    """The oracle, as it stands, on a bounded sample of the step: a 256-page
-    pool of the same model shape, 16 sequences x 4096 tokens gathered for one
-    layer, the 256-token all-layer store, 256 decode tokens stored for one
-    layer, and 512 moved tokens; repeated until `budget_s` has elapsed."""
+def cpu_model() -> str:
+    """Host CPU name, best effort (x86 'model name', Arm implementer/part)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    for line in info.splitlines():
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    parts = {ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU part")}
+    impl = {ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU implementer")}
+    known = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1"}
+    return ", ".join(sorted(known.get(p, f"implementer {','.join(sorted(impl))} part {p}") for p in parts)) or "unknown"
+
+
+def oracle_sample(budget_s: float = 12.0, threads: int = 1):
+    """The oracle, as it stands, on a bounded sample of the step, repeated
+    until `budget_s` has elapsed. One sample: a 256-page pool of the same
+    model shape; translate 512 slots; the 256-token all-layer store; 256
+    decode tokens stored for one layer; 32 sequences x 4096 tokens gathered
+    for one layer; 512 moved tokens. With threads > 1 the sample is split
+    across threads (gather by sequence, all-layer store by layer, the rest by
+    token ranges), all on one shared pool mirror with disjoint writes; the
+    oracle's C routines release the GIL."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle as ora
 
-    P = 256
+    P, n_seq = 256, 32
     sh = SHAPE.scaled(P)
-    o = ora.Oracle(ora.Geometry(sh.layer_num, sh.head_num, sh.head_dim, sh.itemsize, sh.page_size, P))
+    L = sh.layer_num
+    o = ora.Oracle(ora.Geometry(L, sh.head_num, sh.head_dim, sh.itemsize, sh.page_size, P))
     M = synth.sentinel_bytes(5, 0, o.raw_bytes())
     rng = synth.rng_for(sh.seed, synth.S_MISC, 1)
-    ps = sh.page_size
+    ps, R = sh.page_size, sh.row_bytes
     slots = synth.distinct_slots(rng, ps, P * ps, 256 + 256 + 1024)
-    bt = rng.integers(1, P, size=(16, CTX // ps)).astype(np.int32)
-    g = synth.GatherBatch(bt, np.zeros(16, np.int32), np.full(16, CTX, np.int32))
-    kc, vc = synth.kv_pair(sh, sh.layer_num * 256, 1)
+    bt = rng.integers(1, P, size=(n_seq, CTX // ps)).astype(np.int32)
+    kc, vc = synth.kv_pair(sh, L * 256, 1)
+    kc, vc = kc.reshape(L, 256, -1), vc.reshape(L, 256, -1)
     kd, vd = synth.kv_pair(sh, 256, 0)
     src, _ = o.translate(slots[512:1024])
     dst, _ = o.translate(slots[1024:])
-    R = sh.row_bytes
-    outk = np.empty((g.total, R), np.uint8)
-    outv = np.empty((g.total, R), np.uint8)
-    per = useful_bytes(sh, n_decode=256, ctx=CTX, n_chunk=256, n_move=512, n_seqs=16)
-    per_rep = per["translate"] + per["store_all_layers"] + per["store_layer"] // sh.layer_num + \
-        per["gather"] // sh.layer_num + per["move"]
+    outk = np.empty((n_seq * CTX, R), np.uint8)
+    outv = np.empty((n_seq * CTX, R), np.uint8)
+    per = useful_bytes(sh, n_decode=256, ctx=CTX, n_chunk=256, n_move=512, n_seqs=n_seq)
+    per_rep = per["translate"] + per["store_all_layers"] + per["store_layer"] // L + per["gather"] // L + per["move"]
+
+    def rng_of(n, w):
+        k = -(-n // threads)
+        return slice(min(n, w * k), min(n, (w + 1) * k))
+
+    def work(w):
+        a = rng_of(512, w)
+        o.translate(slots[:512][a])
+        for layer in range(w, L, threads):  # all-layer store, split by layer
+            o.store(M, layer, slots[256:512], kc[layer], vc[layer])
+        d = rng_of(256, w)
+        o.store(M, 5, slots[:256][d], kd[d], vd[d])
+        sq = rng_of(n_seq, w)
+        g = synth.GatherBatch(bt[sq], np.zeros(sq.stop - sq.start, np.int32),
+                              np.full(sq.stop - sq.start, CTX, np.int32))
+        r0 = sq.start * CTX
+        o.gather(M, 5, g.block_table, g.seq_len, g.cu + r0, g.seq_start, n_seq * CTX, outk, outv)
+        m = rng_of(512, w)
+        o.move(M, src[m], dst[m])
+
     t0 = time.perf_counter()
     reps = 0
-    while True:
-        o.translate(slots[:512])
-        o.store_all(M, slots[256:512], kc, vc)
-        o.store(M, 5, slots[:256], kd, vd)
-        o.gather(M, 5, g.block_table, g.seq_len, g.cu, g.seq_start, g.total, outk, outv)
-        o.move(M, src, dst)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    return {"value": per_rep * reps / el / GB, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"{reps} reps of: 256-page pool of the same shape; translate 512 slots; store_all 256 "
-                       f"tokens x 32 layers; store_layer 256 tokens; gather 16 seqs x 4096 tokens for one layer; "
-                       f"move 512 tokens; {el:.1f} s single-threaded"),
-            "seconds": el}
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            list(ex.map(work, range(threads)))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    return {"value": per_rep * reps / el / GB, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{reps} reps on {threads} thread(s) of: a 256-page pool of the same shape; translate 512 "
+                       f"slots; store_all 256 tokens x 32 layers; store_layer 256 tokens; gather 32 seqs x 4096 "
+                       f"tokens for one layer; move 512 tokens; {el:.1f} s"),
+            "cpu_model": cpu_model(), "seconds": el}
 
 
 # ------------------------------------------------------------------ ranks
@@ -414,8 +451,12 @@ def run_gpu(args):
         "device_errors": dev_err | bad,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_sample(args.cpu_budget)
-        line["cpu_baseline"].pop("seconds", None)
+        one = oracle_sample(args.cpu_budget / 2, 1)
+        ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        many = oracle_sample(args.cpu_budget / 2, max(1, ncores))
+        many.pop("seconds", None)
+        many["value_1_thread"] = round(one["value"], 3)
+        line["cpu_baseline"] = many
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -431,9 +472,10 @@ def run_reference(args):
 
     oracle.build()
     budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     for _ in range(args.warmup):
-        oracle_sample(budget / 4)
-    vals = [oracle_sample(budget) for _ in range(args.steps)]
+        oracle_sample(budget / 4, ncores)
+    vals = [oracle_sample(budget, ncores) for _ in range(args.steps)]
     v = statistics.mean(x["value"] for x in vals)
     secs = sum(x["seconds"] for x in vals)
     line = {
@@ -443,8 +485,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "kv_dtype": "bf16"},
-        "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": vals[0]["sample"]},
+        "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": ncores, "kind": "oracle",
+                         "sample": vals[0]["sample"], "cpu_model": vals[0]["cpu_model"]},
         "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -455,7 +497,8 @@ def run_reference(args):
 MICRO_DEFAULT = ["translate:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2", "move:2",
                  "translate:3", "store:3", "store_slots:3", "store_all:3", "gather:3",
                  "store:4", "gather:4", "move:4",
-                 "translate:5", "store:5", "store_slots:5", "gather:5", "move:5"]
+                 "translate:5", "store:5", "store_slots:5", "gather:5", "move:5",
+                 "store:6", "store_all:6", "gather:6", "move:6"]
 
 
 def _payload_torch(gen, rows: int, R: int, itemsize: int, dev):
@@ -541,9 +584,10 @@ def run_micro(args):
         sh = synth.SHAPES[cfg]
         if args.pages or args.layers:
             sh = synth.Shape(cfg, sh.name + "-small", args.layers or sh.layer_num, sh.head_num, sh.head_dim,
-                             sh.itemsize, sh.page_size, args.pages or sh.num_pages)
+                             sh.itemsize, sh.page_size, args.pages or sh.num_pages, sh.latent)
         L, R, ps, P = sh.layer_num, sh.row_bytes, sh.page_size, sh.num_pages
-        desc = gt.make_desc(L, sh.head_num, sh.head_dim, sh.itemsize, ps, P)
+        kvr = 1 if sh.latent else 2  # rows per layer per token (MLA: one latent row, no V)
+        desc = gt.make_desc(L, sh.head_num, sh.head_dim, sh.itemsize, ps, P, latent_only=sh.latent)
         total, pad = gt.kv_pool_required_bytes(desc)
         free, _ = torch.cuda.mem_get_info(dev)
         if total + pad + (8 << 30) > free:
@@ -559,7 +603,7 @@ def run_micro(args):
         # The report's own method on the same bytes, for comparison: dense
         # per-layer views over the raw buffer (build_mha_views: block b starts
         # at b*ps*R, rows of R bytes) and torch indexing through them.
-        n_rows_view = P * 2 * L * ps
+        n_rows_view = P * kvr * L * ps
 
         def view(block):
             return torch.as_strided(raw, size=(n_rows_view, R), stride=(R, 1), storage_offset=block * ps * R)
@@ -576,16 +620,17 @@ def run_micro(args):
             report("translate", cfg, f"{n} slots", ms, n * 12, n)
         if "store" in kernels or "store_graph" in kernels or "store_slots" in kernels:
             K = _payload_torch(gen, n, R, sh.itemsize, dev)
-            V = _payload_torch(gen, n, R, sh.itemsize, dev)
-            useful = (n - n_tomb) * 4 * R + n * 4
+            V = None if sh.latent else _payload_torch(gen, n, R, sh.itemsize, dev)
+            useful = (n - n_tomb) * 2 * kvr * R + n * 4
             flush = useful < 4 * l2
             if "store" in kernels:
                 ms = timed(lambda i: gt.kv_store_layer(pool, i % L, ids, K, V), max(calls, L), flush)
                 ids64 = ids.to(torch.int64)
 
                 def ref_store(i):
-                    view(2 * (i % L))[ids64] = K
-                    view(2 * (i % L) + 1)[ids64] = V
+                    view(kvr * (i % L))[ids64] = K
+                    if V is not None:
+                        view(kvr * (i % L) + 1)[ids64] = V
                 ref = timed(ref_store, max(calls, L), flush) if args.torch_ref else None
                 report("store_layer", cfg, f"{n} tokens per layer ({n_tomb} tombstones)", ms, useful, 2 * n,
                        {"l2_flush": flush, "tombstone_bytes": n_tomb * 4 * R}, ref)
@@ -610,11 +655,11 @@ def run_micro(args):
                 del g
             del K, V
         if "store_all" in kernels:
-            na = n if cfg != 2 else 256
+            na = n if cfg not in (2, 6) else 256
             Ka = _payload_torch(gen, L * na, R, sh.itemsize, dev)
-            Va = _payload_torch(gen, L * na, R, sh.itemsize, dev)
+            Va = None if sh.latent else _payload_torch(gen, L * na, R, sh.itemsize, dev)
             ta = int(np.count_nonzero(slots[:na] < 0))
-            useful = L * (na - ta) * 4 * R + na * 4
+            useful = L * (na - ta) * 2 * kvr * R + na * 4
             flush = useful < 4 * l2
             ms = timed(lambda i: gt.kv_store_all_layers(pool, ids[:na], Ka, Va), calls, flush)
             report("store_all_layers", cfg, f"{na} tokens x {L} layers", ms, useful, 2 * L * na,
@@ -626,9 +671,9 @@ def run_micro(args):
                 synth.gather_batch(sh).seq_len[: args.seqs])
             rows = gb.total
             ok = torch.empty((rows, R), dtype=torch.uint8, device=dev)
-            ov = torch.empty_like(ok)
+            ov = None if sh.latent else torch.empty_like(ok)
             bt, ln, cu, st = d(gb.block_table), d(gb.seq_len), d(gb.cu), d(gb.seq_start)
-            useful = rows * 4 * R + rows * 4 // ps
+            useful = rows * 2 * kvr * R + rows * 4 // ps
             flush = useful < 4 * l2
             layers = list(range(L)) if cfg != 5 else [0, L - 1]
             ms = timed(lambda i: gt.kv_gather_layer(pool, layers[i % len(layers)], bt, ln, cu, ok, ov, st),
@@ -638,12 +683,13 @@ def run_micro(args):
                 # view rows of every output token, precomputed (not timed)
                 seq = np.repeat(np.arange(gb.block_table.shape[0]), gb.seq_len - gb.seq_start)
                 j = np.concatenate([np.arange(a, b) for a, b in zip(gb.seq_start, gb.seq_len)])
-                vrow = torch.from_numpy(gb.block_table[seq, j // ps].astype(np.int64) * (2 * L * ps) + j % ps).to(dev)
+                vrow = torch.from_numpy(gb.block_table[seq, j // ps].astype(np.int64) * (kvr * L * ps) + j % ps).to(dev)
 
                 def ref_gather(i):
                     layer = layers[i % len(layers)]
-                    torch.index_select(view(2 * layer), 0, vrow, out=ok)
-                    torch.index_select(view(2 * layer + 1), 0, vrow, out=ov)
+                    torch.index_select(view(kvr * layer), 0, vrow, out=ok)
+                    if ov is not None:
+                        torch.index_select(view(kvr * layer + 1), 0, vrow, out=ov)
                 ref = timed(ref_gather, max(calls, len(layers)), flush)
             distinct = len(np.unique(gb.block_table))
             report("gather_layer", cfg, f"{gb.block_table.shape[0]} seqs, {rows} rows", ms, useful, rows,
@@ -655,7 +701,7 @@ def run_micro(args):
             m = src.size
             mv = torch.empty(2 * m, dtype=torch.int32, device=dev)
             gt.kv_translate(pool, d(np.concatenate([src, dst])), mv)
-            useful = m * (2 * L * R * 2 + 8)
+            useful = m * (kvr * L * R * 2 + 8)
             flush = useful < 4 * l2
             ms = timed(lambda i: gt.kv_move(pool, mv[:m], mv[m:]), calls, flush)
             ref = None
@@ -663,11 +709,11 @@ def run_micro(args):
                 s64, d64 = mv[:m].to(torch.int64), mv[m:].to(torch.int64)
 
                 def ref_move(i):  # every layer's K and V view, one indexing op each
-                    for b in range(2 * L):
+                    for b in range(kvr * L):
                         vb = view(b)
                         vb[d64] = vb[s64]
                 ref = timed(ref_move, max(3, calls // 4), flush)
-            report("move", cfg, f"{m} tokens x {2 * L} row-blocks", ms, useful, 2 * L * m, {"l2_flush": flush}, ref)
+            report("move", cfg, f"{m} tokens x {kvr * L} row-blocks", ms, useful, kvr * L * m, {"l2_flush": flush}, ref)
         err = gt.kv_pool_last_error(pool)
         assert err == 0, f"device error bits {err}"
         gt.kv_pool_destroy(pool)

@@ -48,6 +48,8 @@ class kv_pool_desc(ctypes.Structure):
         ("page_size", ctypes.c_int32),
         ("num_pages", ctypes.c_int64),
         ("anchor_bytes", ctypes.c_int64),
+        ("latent_only", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -63,13 +65,17 @@ class kv_pool_info_t(ctypes.Structure):
         ("last_view_end", ctypes.c_int64),
         ("device", ctypes.c_int32),
         ("owns_raw", ctypes.c_int32),
+        ("blocks_per_page", ctypes.c_int32),
+        ("latent_only", ctypes.c_int32),
     ]
 
 
 def make_desc(layer_num, head_num, head_dim, itemsize, page_size, num_pages, anchor_bytes=0,
-              v_head_dim=None) -> kv_pool_desc:
+              v_head_dim=None, latent_only=False) -> kv_pool_desc:
+    """Pool geometry; latent_only=True makes an MLA pool (one latent row of
+    head_num * head_dim elements per layer per token, no V)."""
     return kv_pool_desc(layer_num, head_num, head_dim, head_dim if v_head_dim is None else v_head_dim,
-                        itemsize, page_size, num_pages, anchor_bytes)
+                        itemsize, page_size, num_pages, anchor_bytes, 1 if latent_only else 0, 0)
 
 
 _lib = None
@@ -214,7 +220,7 @@ def kv_translate(pool: KVPool, slots: torch.Tensor, ids_out: torch.Tensor, v2p: 
     return ids_out
 
 
-def kv_store_layer(pool: KVPool, layer: int, ids: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+def kv_store_layer(pool: KVPool, layer: int, ids: torch.Tensor, k: torch.Tensor, v: torch.Tensor | None,
                    stream=None) -> None:
     n = ids.numel()
     nb = n * pool.row_bytes
@@ -223,7 +229,7 @@ def kv_store_layer(pool: KVPool, layer: int, ids: torch.Tensor, k: torch.Tensor,
         _stream(stream)))
 
 
-def kv_store_all_layers(pool: KVPool, ids: torch.Tensor, k_all: torch.Tensor, v_all: torch.Tensor,
+def kv_store_all_layers(pool: KVPool, ids: torch.Tensor, k_all: torch.Tensor, v_all: torch.Tensor | None,
                         stream=None) -> None:
     n = ids.numel()
     nb = pool.desc.layer_num * n * pool.row_bytes
@@ -232,7 +238,7 @@ def kv_store_all_layers(pool: KVPool, ids: torch.Tensor, k_all: torch.Tensor, v_
         _dev(v_all, "v_all", nbytes=nb), _stream(stream)))
 
 
-def kv_store_layer_slots(pool: KVPool, layer: int, slots: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+def kv_store_layer_slots(pool: KVPool, layer: int, slots: torch.Tensor, k: torch.Tensor, v: torch.Tensor | None,
                          v2p: torch.Tensor | None = None, stream=None) -> None:
     n = slots.numel()
     nb = n * pool.row_bytes
@@ -241,7 +247,7 @@ def kv_store_layer_slots(pool: KVPool, layer: int, slots: torch.Tensor, k: torch
         0 if v2p is None else v2p.numel(), _dev(k, "k", nbytes=nb), _dev(v, "v", nbytes=nb), _stream(stream)))
 
 
-def kv_store_all_layers_slots(pool: KVPool, slots: torch.Tensor, k_all: torch.Tensor, v_all: torch.Tensor,
+def kv_store_all_layers_slots(pool: KVPool, slots: torch.Tensor, k_all: torch.Tensor, v_all: torch.Tensor | None,
                               v2p: torch.Tensor | None = None, stream=None) -> None:
     n = slots.numel()
     nb = pool.desc.layer_num * n * pool.row_bytes
@@ -252,7 +258,7 @@ def kv_store_all_layers_slots(pool: KVPool, slots: torch.Tensor, k_all: torch.Te
 
 
 def kv_gather_layer(pool: KVPool, layer: int, block_table: torch.Tensor, seq_len: torch.Tensor,
-                    cu_out: torch.Tensor, out_k: torch.Tensor, out_v: torch.Tensor,
+                    cu_out: torch.Tensor, out_k: torch.Tensor, out_v: torch.Tensor | None,
                     seq_start: torch.Tensor | None = None, stream=None) -> None:
     if block_table.dim() != 2:
         raise ValueError("block_table must be [n_seqs, max_pages]")
@@ -263,7 +269,7 @@ def kv_gather_layer(pool: KVPool, layer: int, block_table: torch.Tensor, seq_len
         raise ValueError("seq_start must be [n_seqs]")
     R = pool.row_bytes
     ob = out_k.numel() * out_k.element_size()
-    if ob % R != 0 or out_v.numel() * out_v.element_size() != ob:
+    if ob % R != 0 or (out_v is not None and out_v.numel() * out_v.element_size() != ob):
         raise ValueError("out_k and out_v must be the same size, a whole number of rows")
     _check("kv_gather_layer", lib().kv_gather_layer(
         pool.handle, layer, _dev(block_table, "block_table", torch.int32), n_seqs, max_pages,

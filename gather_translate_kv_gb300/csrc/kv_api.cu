@@ -126,6 +126,7 @@ int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, k
   d.n_rows = lay.n_rows;
   d.num_pages = desc->num_pages;
   d.blocks = static_cast<int32_t>(lay.blocks);
+  d.kv_rows = static_cast<int32_t>(lay.kv_rows);
   d.ps_shift = ps_shift_of(desc->page_size);
   d.err = p->d_err;
   *out = p;
@@ -153,6 +154,8 @@ int kv_pool_info(const kv_pool_t* pool, kv_pool_info_t* out) {
   out->last_view_end = pool->lay.last_view_end;
   out->device = pool->device;
   out->owns_raw = pool->owns_raw;
+  out->blocks_per_page = static_cast<int32_t>(pool->lay.blocks);
+  out->latent_only = pool->desc.latent_only;
   return KV_OK;
 }
 
@@ -179,7 +182,8 @@ int kv_store_layer(const kv_pool_t* pool, int32_t layer, const int32_t* ids_dev,
   if (rc != KV_OK) return rc;
   if (n < 0 || layer < 0 || layer >= pool->desc.layer_num) return KV_ERR_INVALID;
   if (n == 0) return KV_OK;
-  if (ids_dev == nullptr || k_dev == nullptr || v_dev == nullptr) return KV_ERR_INVALID;
+  if (pool->desc.latent_only) v_dev = nullptr;  // MLA: no V rows
+  if (ids_dev == nullptr || k_dev == nullptr || (v_dev == nullptr && !pool->desc.latent_only)) return KV_ERR_INVALID;
   if (!aligned16(k_dev) || !aligned16(v_dev) || (reinterpret_cast<uintptr_t>(ids_dev) & 3u)) return KV_ERR_ALIGN;
   return launched(gtkv::launch_store(pool->dev, layer, 1, ids_dev, n, k_dev, v_dev, pool->sm_count,
                                      as_stream(stream)));
@@ -191,7 +195,9 @@ int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n
   if (rc != KV_OK) return rc;
   if (n < 0) return KV_ERR_INVALID;
   if (n == 0) return KV_OK;
-  if (ids_dev == nullptr || k_all_dev == nullptr || v_all_dev == nullptr) return KV_ERR_INVALID;
+  if (pool->desc.latent_only) v_all_dev = nullptr;
+  if (ids_dev == nullptr || k_all_dev == nullptr || (v_all_dev == nullptr && !pool->desc.latent_only))
+    return KV_ERR_INVALID;
   if (!aligned16(k_all_dev) || !aligned16(v_all_dev) || (reinterpret_cast<uintptr_t>(ids_dev) & 3u))
     return KV_ERR_ALIGN;
   return launched(gtkv::launch_store(pool->dev, 0, pool->desc.layer_num, ids_dev, n, k_all_dev, v_all_dev,
@@ -205,7 +211,9 @@ static int store_slots(const kv_pool_t* pool, int32_t layer0, int32_t n_layers, 
   if (rc != KV_OK) return rc;
   if (n < 0 || v2p_len < 0) return KV_ERR_INVALID;
   if (n == 0) return KV_OK;
-  if (slots_dev == nullptr || k_dev == nullptr || v_dev == nullptr || (v2p_dev == nullptr && v2p_len > 0))
+  if (pool->desc.latent_only) v_dev = nullptr;
+  if (slots_dev == nullptr || k_dev == nullptr || (v_dev == nullptr && !pool->desc.latent_only) ||
+      (v2p_dev == nullptr && v2p_len > 0))
     return KV_ERR_INVALID;
   if (!aligned16(k_dev) || !aligned16(v_dev) || (reinterpret_cast<uintptr_t>(slots_dev) & 7u) ||
       (reinterpret_cast<uintptr_t>(v2p_dev) & 3u))
@@ -238,7 +246,9 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
   if (n_seqs == 0) return KV_OK;
   if (seq_len_dev == nullptr || cu_out_dev == nullptr || (block_table_dev == nullptr && max_pages > 0))
     return KV_ERR_INVALID;
-  if (out_rows > 0 && (out_k_dev == nullptr || out_v_dev == nullptr)) return KV_ERR_INVALID;
+  if (pool->desc.latent_only) out_v_dev = nullptr;  // MLA: no V output
+  if (out_rows > 0 && (out_k_dev == nullptr || (out_v_dev == nullptr && !pool->desc.latent_only)))
+    return KV_ERR_INVALID;
   if ((out_k_dev && !aligned16(out_k_dev)) || (out_v_dev && !aligned16(out_v_dev)) ||
       (reinterpret_cast<uintptr_t>(cu_out_dev) & 7u) || (reinterpret_cast<uintptr_t>(seq_len_dev) & 3u) ||
       (reinterpret_cast<uintptr_t>(block_table_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_start_dev) & 3u))

@@ -3,7 +3,8 @@
 // Every kernel here is a row mover: a row is R = H*D*itemsize bytes (one
 // token's K or V for one layer), copied as R/16 16-byte vectors. G lanes of a
 // warp cooperate on one row (G = min(32, R/16) for the common power-of-two
-// rows), each lane holding VPL vectors of it; a warp thus covers 32/G rows
+// rows; 8 lanes x 9 vectors for 1152-byte MLA latents), each lane holding
+// VPL vectors of it; a warp thus covers 32/G rows
 // per wave, and U waves are loaded into registers before any is stored so
 // that every lane keeps several 16-byte loads in flight. All byte offsets are
 // 64-bit: a pool reaches 1.3e11 bytes while ids stay below 2^31.
@@ -28,7 +29,8 @@ struct DevPool {
   int64_t stride;     // rows per page envelope, ps * 2L
   int64_t n_rows;     // num_pages * 2L * ps
   int64_t num_pages;  // P
-  int32_t blocks;     // 2L
+  int32_t blocks;     // row-blocks per page: 2L, or L for an MLA pool
+  int32_t kv_rows;    // rows per layer per token: 2 (K then V) or 1 (MLA latent)
   int32_t ps_shift;   // log2(ps) when ps is a power of two, else -1
   int32_t* err;       // device error word (KV_DEV_ERR_* bits)
 };
@@ -211,7 +213,7 @@ __device__ __forceinline__ void copy_rows(const uint4* const (&src)[N], uint4* c
 #endif
 
 // Row geometry chosen on the host from R/16; the list of instantiations.
-enum class RowKind { V4, V8, V16, V32, V64, V128, V256, Dyn };
+enum class RowKind { V4, V8, V16, V32, V64, V72, V96, V128, V256, Dyn };
 
 inline RowKind row_kind(int64_t vpr) {
   switch (vpr) {
@@ -220,6 +222,8 @@ inline RowKind row_kind(int64_t vpr) {
     case 16: return RowKind::V16;
     case 32: return RowKind::V32;
     case 64: return RowKind::V64;
+    case 72: return RowKind::V72;   // 1152-byte rows: an MLA latent of 576 bf16
+    case 96: return RowKind::V96;   // 1536-byte rows
     case 128: return RowKind::V128;
     case 256: return RowKind::V256;
     default: return RowKind::Dyn;
@@ -235,6 +239,8 @@ inline cudaError_t dispatch_row(int64_t vpr, F&& f) {
     case RowKind::V16: return f.template operator()<16, 1>();
     case RowKind::V32: return f.template operator()<32, 1>();
     case RowKind::V64: return f.template operator()<32, 2>();
+    case RowKind::V72: return f.template operator()<8, 9>();
+    case RowKind::V96: return f.template operator()<32, 3>();
     case RowKind::V128: return f.template operator()<32, 4>();
     case RowKind::V256: return f.template operator()<32, 8>();
     default: return f.template operator()<32, 0>();

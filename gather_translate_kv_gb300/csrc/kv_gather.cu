@@ -5,6 +5,9 @@
 // layout/page_major.py): token (page p, offset o) of layer l is K-view row
 // p*ps*2L + o + 2l*ps, and its V row follows ps rows later.
 //
+// In an MLA pool (one latent row per layer, L row-blocks per page) layer l is
+// block l and there is no V output.
+//
 // The block table is the work list. Entry (s, k) covers tokens
 // [k*ps, (k+1)*ps) of sequence s; clipped to the window [start_s, len_s) it is
 // a run of consecutive pool rows (one page's block 2l, then the same run in
@@ -51,7 +54,8 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
 
   const int lane = threadIdx.x & 31;
   const int64_t vpr = p.vpr;
-  const int64_t koff = 2 * static_cast<int64_t>(layer) * ps;
+  const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * ps;  // K (or latent) block of the layer
+  const bool has_v = p.kv_rows == 2;
   const int64_t n_items = static_cast<int64_t>(n_seqs) * max_pages * chunks_per_page;
   const L2Policy pol = make_l2_policy();
 
@@ -85,7 +89,7 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
     if (rlo >= rhi) continue;
     const int64_t nvec = (rhi - rlo) * vpr;
     uint4* dk = out_k + rlo * vpr;
-    uint4* dv = out_v + rlo * vpr;
+    uint4* dv = has_v ? out_v + rlo * vpr : nullptr;
     if (page >= 0) {
       const uint4* srck = p.base + (page * p.stride + koff + (jlo - k * ps)) * vpr;
       const uint4* srcv = srck + ps * vpr;
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
           const int64_t v = v0 + lane + 32 * i;
           if (v < nvec) {
             bk[i] = ld16<GTKV_GATHER_LD>(srck + v, pol);
-            bv[i] = ld16<GTKV_GATHER_LD>(srcv + v, pol);
+            if (has_v) bv[i] = ld16<GTKV_GATHER_LD>(srcv + v, pol);
           }
         }
 #pragma unroll
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
           const int64_t v = v0 + lane + 32 * i;
           if (v < nvec) {
             st16<GTKV_GATHER_ST>(dk + v, bk[i], pol);
-            st16<GTKV_GATHER_ST>(dv + v, bv[i], pol);
+            if (has_v) st16<GTKV_GATHER_ST>(dv + v, bv[i], pol);
           }
         }
       }
@@ -114,10 +118,230 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
       for (int64_t v = lane; v < nvec; v += 32) {
         const int64_t col = v % vpr;
         st16<GTKV_GATHER_ST>(dk + v, ld16<GTKV_GATHER_LD>(srck + col, pol), pol);
-        st16<GTKV_GATHER_ST>(dv + v, ld16<GTKV_GATHER_LD>(srcv + col, pol), pol);
+        if (has_v) st16<GTKV_GATHER_ST>(dv + v, ld16<GTKV_GATHER_LD>(srcv + col, pol), pol);
       }
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Bulk-copy form of the same gather (cp.async.bulk, the Hopper/Blackwell
+// bulk-copy engine): every warp runs one single-thread pipeline that stages
+// each chunk global -> shared (K and V, completion counted on an mbarrier)
+// and writes it back shared -> global with bulk stores, keeping up to
+// GTKV_BULK_STAGES - 1 chunks in flight. Items, clipping and error bits are
+// those of k_gather_runs. Used when a chunk fits its stage (R <= 4 KiB).
+#ifndef GTKV_GATHER_BULK
+#define GTKV_GATHER_BULK 0
+#endif
+#ifndef GTKV_BULK_WARPS
+#define GTKV_BULK_WARPS 4
+#endif
+#ifndef GTKV_BULK_STAGES
+#define GTKV_BULK_STAGES 4
+#endif
+constexpr int kBulkHalf = GTKV_GATHER_CHUNK;          // bytes of K (or V) a stage holds
+constexpr int kBulkStage = 2 * kBulkHalf;             // K then V
+constexpr unsigned kBulkSpinLimit = 1u << 24;         // mbarrier polls before giving up (~1 s)
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for a stage's loads: non-blocking polls with a short sleep,
+// at most kBulkSpinLimit of them (about a second); false = gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (unsigned spins = 0; spins < kBulkSpinLimit; ++spins) {
+    if (mbar_test_wait(bar, parity)) return true;
+    __nanosleep(32);
+  }
+  return false;
+}
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_addr(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+               "r"(smem_addr(ssrc)), "r"(bytes), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
+    DevPool p, int32_t layer, const int32_t* __restrict__ bt, int32_t n_seqs, int32_t max_pages,
+    const int32_t* __restrict__ seq_start, const int32_t* __restrict__ seq_len, const int64_t* __restrict__ cu,
+    uint4* __restrict__ out_k, uint4* __restrict__ out_v, int64_t out_rows, int32_t chunk_rows,
+    int32_t chunks_per_page) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int D = GTKV_BULK_STAGES;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t ps = p.ps;
+  for (int64_t s = tid; s < n_seqs; s += nthreads) {
+    const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
+    const int64_t b = __ldg(seq_len + s);
+    const int64_t c0 = __ldg(cu + s), c1 = __ldg(cu + s + 1);
+    if (a < 0 || b > static_cast<int64_t>(max_pages) * ps || c0 < 0 || c1 < c0 || c1 - c0 < b - a)
+      atomicOr(p.err, KV_DEV_ERR_TABLE);
+  }
+  if (tid == 0 && __ldg(cu + n_seqs) > out_rows) atomicOr(p.err, KV_DEV_ERR_TABLE);
+
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  uint8_t* buf = smem + static_cast<size_t>(wib) * D * kBulkStage;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(GTKV_BULK_WARPS) * D * kBulkStage) + wib * D;
+  if (lane == 0) {
+    for (int i = 0; i < D; ++i) mbar_init(bar + i);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncwarp();
+
+  const int64_t vpr = p.vpr;
+  const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * ps;
+  const bool has_v = p.kv_rows == 2;
+  const int64_t n_items = static_cast<int64_t>(n_seqs) * max_pages * chunks_per_page;
+  const int64_t it_step = nthreads >> 5;
+  const L2Policy pol = make_l2_policy();
+
+  // Pipeline state, uniform across the warp; lane 0 issues every bulk copy.
+  int64_t q_src[D];  // per stage: source (vector index from p.base), destination row, bytes
+  int64_t q_row[D];
+  uint32_t q_bytes[D];
+  int head = 0, tail = 0;  // items loaded / items stored
+  bool failed = false;
+
+  auto issue = [&](int st, int64_t src, int64_t row, uint32_t bytes) {
+    q_src[st] = src;
+    q_row[st] = row;
+    q_bytes[st] = bytes;
+    if (lane == 0) {
+      uint8_t* sb = buf + st * kBulkStage;
+      mbar_expect_tx(bar + st, has_v ? 2 * bytes : bytes);
+      bulk_load(sb, p.base + src, bytes, bar + st, pol.keep);
+      if (has_v) bulk_load(sb + kBulkHalf, p.base + src + ps * vpr, bytes, bar + st, pol.keep);
+    }
+  };
+  // Store the oldest loaded item; false when its load never landed.
+  auto retire = [&]() -> bool {
+    const int st = tail % D;
+    bool ok = true;
+    if (lane == 0) {
+      ok = mbar_wait_bounded(bar + st, (tail / D) & 1);
+      if (ok) {
+        uint8_t* sb = buf + st * kBulkStage;
+        bulk_store(out_k + q_row[st] * vpr, sb, q_bytes[st], pol.first);
+        if (has_v) bulk_store(out_v + q_row[st] * vpr, sb + kBulkHalf, q_bytes[st], pol.first);
+        bulk_commit();
+      }
+    }
+    ok = __shfl_sync(kFull, ok, 0);
+    ++tail;
+    return ok;
+  };
+
+  for (int64_t base = tid >> 5; base < n_items && !failed; base += 32 * it_step) {
+    // lane k works out item base + k*step: empty, an error, a sink run, or a bulk run
+    const int64_t it = base + lane * it_step;
+    int64_t src = -1, row = 0;
+    uint32_t bytes = 0;
+    bool sink = false;
+    if (it < n_items) {
+      const int64_t sk = it / chunks_per_page;
+      const int64_t c = it - sk * chunks_per_page;
+      const int64_t s = sk / max_pages;
+      const int64_t k = sk - s * max_pages;
+      const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
+      const int64_t b = __ldg(seq_len + s);
+      const int64_t j0 = k * ps + c * chunk_rows;
+      int64_t jlo = j0 > a ? j0 : a;
+      if (jlo < 0) jlo = 0;
+      int64_t jhi = j0 + chunk_rows;
+      if (jhi > (k + 1) * ps) jhi = (k + 1) * ps;
+      if (jhi > b) jhi = b;
+      if (jlo < jhi) {
+        const int64_t page = __ldg(bt + sk);
+        if (page >= p.num_pages) {
+          atomicOr(p.err, KV_DEV_ERR_ROW);
+        } else {
+          const int64_t cs = __ldg(cu + s);
+          int64_t rlo = cs + (jlo - a);
+          int64_t rhi = cs + (jhi - a);
+          if (rlo < 0) {
+            jlo -= rlo;
+            rlo = 0;
+          }
+          if (rhi > out_rows) rhi = out_rows;
+          if (rlo < rhi) {
+            row = rlo;
+            bytes = static_cast<uint32_t>((rhi - rlo) * vpr * 16);
+            if (page < 0) {
+              sink = true;
+              src = koff * vpr;
+            } else {
+              src = (page * p.stride + koff + (jlo - k * ps)) * vpr;
+            }
+          }
+        }
+      }
+    }
+    unsigned todo = __ballot_sync(kFull, src >= 0);
+    while (todo) {
+      const int k = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const long long isrc = __shfl_sync(kFull, src, k);
+      const long long irow = __shfl_sync(kFull, row, k);
+      const uint32_t ibytes = __shfl_sync(kFull, bytes, k);
+      if (__shfl_sync(kFull, sink, k)) {  // tombstoned entry: rows read the sink, copied by the warp
+        const int64_t nvec = ibytes / 16;
+        for (int64_t v = lane; v < nvec; v += 32) {
+          out_k[irow * vpr + v] = ld16<kLdNc>(p.base + isrc + v % vpr, pol);
+          if (has_v) out_v[irow * vpr + v] = ld16<kLdNc>(p.base + isrc + ps * vpr + v % vpr, pol);
+        }
+        continue;
+      }
+      if (head - tail == D) {  // every stage busy: retire the oldest, then reuse its stage
+        if (!retire()) {
+          failed = true;
+          break;
+        }
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
+      issue(head % D, isrc, irow, ibytes);
+      ++head;
+    }
+  }
+  while (!failed && tail < head) {
+    if (!retire()) failed = true;
+  }
+  if (failed && lane == 0) {  // a load never landed: report, wait (bounded) for the others, drain
+    atomicOr(p.err, KV_DEV_ERR_TIMEOUT);
+    for (int u = tail; u < head; ++u) mbar_wait_bounded(bar + u % D, (u / D) & 1);
+  }
+  if (lane == 0) bulk_wait_all();
 }
 
 }  // namespace
@@ -130,6 +354,28 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
   if (chunk_rows < 1) chunk_rows = 1;
   if (chunk_rows > p.ps) chunk_rows = p.ps;
   const int64_t cpp = (p.ps + chunk_rows - 1) / chunk_rows;
+  if (GTKV_GATHER_BULK && chunk_rows * 16 * p.vpr <= kBulkHalf) {
+    constexpr int threads = 32 * GTKV_BULK_WARPS;
+    constexpr size_t smem = static_cast<size_t>(GTKV_BULK_WARPS) * GTKV_BULK_STAGES * (kBulkStage + 8);
+    static bool attr = false;
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(k_gather_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_gather_bulk, threads, smem) != cudaSuccess || nb < 1)
+      nb = 1;
+    int64_t blocks = (static_cast<int64_t>(n_seqs) * max_pages * cpp + GTKV_BULK_WARPS - 1) / GTKV_BULK_WARPS;
+    const int64_t cap = static_cast<int64_t>(sm_count) * nb;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    k_gather_bulk<<<static_cast<unsigned>(blocks), threads, smem, s>>>(
+        p, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu, static_cast<uint4*>(out_k),
+        static_cast<uint4*>(out_v), out_rows, static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp));
+    return cudaGetLastError();
+  }
   auto kernel = k_gather_runs<CHV>;
   int64_t warps = static_cast<int64_t>(n_seqs) * max_pages * cpp;
   const int64_t seq_warps = (static_cast<int64_t>(n_seqs) + 31) / 32;

@@ -12,8 +12,9 @@ namespace gtkv {
 
 struct Layout {
   int64_t R;              // row bytes, H * D * itemsize
-  int64_t blocks;         // 2L row-blocks per page
-  int64_t page_bytes;     // ps * 2L * R
+  int64_t blocks;         // row-blocks per page: 2L (MHA/SWA) or L (MLA)
+  int64_t kv_rows;        // rows per layer per token: 2 (K, V) or 1 (MLA latent)
+  int64_t page_bytes;     // ps * blocks * R
   int64_t total;          // num_pages * page_bytes
   int64_t tail_pad;       // ps * 2L * R (one page envelope)
   int64_t n_rows;         // num_pages * 2L * ps

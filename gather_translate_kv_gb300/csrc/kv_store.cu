@@ -7,7 +7,9 @@
 //
 // In view terms, token id's K row of layer l is pool row id + 2l*ps and its V
 // row id + (2l+1)*ps. A task is one (layer, token) pair; it moves 2 rows in
-// (contiguous K/V inputs) and 2 rows out (scattered pool rows).
+// (contiguous K/V inputs) and 2 rows out (scattered pool rows). In an MLA pool
+// (one latent row per layer, blocks_per_page = L) the row is id + l*ps and
+// there is no V.
 #include "kv_common.cuh"
 
 namespace gtkv {
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(kBlock) k_store(DevPool p, int32_t layer0, int
     long long row = -1;  // K row of this lane's task, in view units; -1 = skip
     if (t < n_tasks) {
       if (id >= 0 && id < p.n_rows) {
-        row = id + 2 * (layer0 + l) * p.ps;
+        row = id + (layer0 + l) * p.kv_rows * p.ps;
       } else {
         atomicOr(p.err, KV_DEV_ERR_ROW);
       }
@@ -87,9 +89,10 @@ __global__ void __launch_bounds__(kBlock) k_store(DevPool p, int32_t layer0, int
         const bool ok = j < cnt && rr >= 0;
         const int64_t tt = ok ? t0 + j : 0;
         const int64_t r_ = ok ? rr : 0;
-        go[2 * u] = go[2 * u + 1] = ok;
+        go[2 * u] = ok;
+        go[2 * u + 1] = ok && V != nullptr;  // an MLA pool has no V rows
         src[2 * u] = K + tt * vpr;
-        src[2 * u + 1] = V + tt * vpr;
+        src[2 * u + 1] = (V != nullptr ? V : K) + tt * vpr;
         dst[2 * u] = p.base + r_ * vpr;
         dst[2 * u + 1] = p.base + (r_ + p.ps) * vpr;
       }

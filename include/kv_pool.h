@@ -44,6 +44,12 @@
  *    KV_DEV_ERR_* bit into the pool's device error word, which
  *    kv_pool_last_error returns and clears.
  *  - K/V bytes are opaque: no call converts, rounds or inspects them.
+ *
+ * MLA pools (latent_only = 1). The report's MLA sub-pools use the same dense
+ * per-layer views with blocks_per_page() = layer_num (实现拆解 step 2): the
+ * envelope is [L0 | L1 | ...], one latent row per layer per token, layer l
+ * in block l, kernel_id(t) = (t / ps) * (ps * L) + t % ps. Everything above
+ * holds with 2L replaced by L; every V argument is ignored (may be NULL).
  */
 #ifndef GATHER_TRANSLATE_KV_GB300_KV_POOL_H
 #define GATHER_TRANSLATE_KV_GB300_KV_POOL_H
@@ -71,6 +77,7 @@ enum {
 #define KV_DEV_ERR_V2P 2   /* translate: a virtual page index was past the page map        */
 #define KV_DEV_ERR_TABLE 4 /* gather: sequence metadata inconsistent (see kv_gather_layer) */
 #define KV_DEV_ERR_FORM 8  /* move: an id was not p * ps * 2L + o with o < ps; pair skipped */
+#define KV_DEV_ERR_TIMEOUT 16 /* an asynchronous copy did not complete in time; the kernel stopped */
 
 typedef struct kv_pool kv_pool_t; /* opaque, host-side, owned by the library */
 
@@ -87,6 +94,10 @@ typedef struct {
   int32_t page_size;    /* ps >= 1 tokens per page                                 */
   int64_t num_pages;    /* P >= 1; page 0 is the tombstone sink                    */
   int64_t anchor_bytes; /* byte offset of the pool in the raw buffer, % 16 == 0    */
+  int32_t latent_only;  /* 0: MHA/SWA pool, a K and a V row per layer (2L blocks)  */
+                        /* 1: MLA pool, one latent row per layer (L blocks, no V;  */
+                        /*    v_head_dim is ignored). Zero-initialised = MHA.      */
+  int32_t reserved;     /* must be 0                                               */
 } kv_pool_desc;
 
 /* Derived layout of a pool (kv_pool_info). */
@@ -101,6 +112,8 @@ typedef struct {
   int64_t last_view_end; /* anchor + (2L-1)*ps*R + n_rows*R               */
   int32_t device;        /* CUDA device ordinal the pool lives on         */
   int32_t owns_raw;      /* 1 when kv_pool_create allocated the buffer    */
+  int32_t blocks_per_page; /* 2L (MHA/SWA) or L (MLA)                     */
+  int32_t latent_only;   /* the descriptor's flag                         */
 } kv_pool_info_t;
 
 /* Sizes of a pool, host only, no CUDA call.

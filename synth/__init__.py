@@ -157,6 +157,7 @@ class Shape:
     itemsize: int
     page_size: int
     num_pages: int
+    latent: bool = False  # MLA pool: one latent row (head_num * head_dim) per layer per token
 
     @property
     def seed(self) -> int:
@@ -173,7 +174,7 @@ class Shape:
     def scaled(self, num_pages: int) -> "Shape":
         """Same model shape on a smaller pool (for element-by-element tests)."""
         return Shape(self.cfg, self.name + f"@P{num_pages}", self.layer_num, self.head_num,
-                     self.head_dim, self.itemsize, self.page_size, num_pages)
+                     self.head_dim, self.itemsize, self.page_size, num_pages, self.latent)
 
 
 SHAPES = {
@@ -182,6 +183,8 @@ SHAPES = {
     3: Shape(3, "llama3-8b-prefill", 32, 8, 128, 2, 64, 4096),
     4: Shape(4, "swa-fp8", 24, 8, 64, 1, 32, 16384),
     5: Shape(5, "id-bound-stress-fp8", 80, 1, 64, 1, 256, 48828),
+    # MLA pool (DeepSeek-like latent 512 + 64 rope, bf16, 61 layers), ~8 GiB
+    6: Shape(6, "mla-deepseek-like", 61, 1, 576, 2, 64, 1820, latent=True),
 }
 
 
@@ -252,7 +255,7 @@ def store_slots(shape: Shape, layer: int, n: int | None = None) -> np.ndarray:
         n = 100 if n is None else n
         s = rng.permutation(np.arange(ps, 256 if P == 64 else P * ps, dtype=np.int64))[:n]
         return with_tombstones(rng_for(shape.seed, S_TOMB, layer), s, max(1, n // 20))
-    if shape.cfg == 2:
+    if shape.cfg in (2, 6):
         n = 256 if n is None else n
         return distinct_slots(rng, ps, P * ps, n)
     if shape.cfg == 3:
@@ -317,6 +320,10 @@ def gather_batch(shape: Shape) -> GatherBatch:
         npg = min(npg, P - 1)
         bt = np.stack([1 + rng.permutation(P - 1)[:npg] for _ in range(S)]).astype(np.int32)
         return GatherBatch(bt, np.zeros(S, np.int32), np.full(S, npg * ps, np.int32))
+    if shape.cfg == 6:
+        S, npg = 128, min(64, P - 1)
+        bt = np.stack([1 + rng.permutation(P - 1)[:npg] for _ in range(S)]).astype(np.int32)
+        return GatherBatch(bt, np.zeros(S, np.int32), np.full(S, npg * ps, np.int32))
     if shape.cfg == 3:
         _, bt = prefill_slots(shape)
         S = bt.shape[0]
@@ -337,7 +344,7 @@ def move_slots(shape: Shape, m: int | None = None, avoid: np.ndarray | None = No
     ps, P = shape.page_size, shape.num_pages
     rng = rng_for(shape.seed, S_MOVE, 0)
     if m is None:
-        m = {1: 20, 2: 8192, 3: 8192, 4: 8192, 5: 8192}[shape.cfg]
+        m = {1: 20, 2: 8192, 3: 8192, 4: 8192, 5: 8192, 6: 4096}.get(shape.cfg, 256)
     if avoid is not None and avoid.size:
         pool = np.setdiff1d(np.arange(ps, P * ps, dtype=np.int64), avoid)
         dst = rng.choice(pool, size=m, replace=False)

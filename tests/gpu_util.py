@@ -36,10 +36,11 @@ class PoolPair:
     a host mirror of the same bytes for the oracle."""
 
     def __init__(self, shape: synth.Shape, anchor: int = 0, fill_seed: int = 4242, mirror: bool = True,
-                 device: str = "cuda"):
+                 device: str = "cuda", latent: bool = False):
         self.shape = shape
+        self.latent = latent
         self.geom = oracle.Geometry(shape.layer_num, shape.head_num, shape.head_dim, shape.itemsize,
-                                    shape.page_size, shape.num_pages, anchor)
+                                    shape.page_size, shape.num_pages, anchor, latent_only=latent)
         self.o = oracle.Oracle(self.geom)
         self.sizes = self.o.sizes()
         self.R = self.sizes["row_bytes"]
@@ -49,12 +50,12 @@ class PoolPair:
         synth.fill_sentinel_torch(self.raw, fill_seed)
         self.M = synth.sentinel_bytes(fill_seed, 0, self.nbytes) if mirror else None
         self.desc = gt.make_desc(shape.layer_num, shape.head_num, shape.head_dim, shape.itemsize,
-                                 shape.page_size, shape.num_pages, anchor)
+                                 shape.page_size, shape.num_pages, anchor, latent_only=latent)
         self.pool = gt.kv_pool_create(self.desc, self.raw)
         self.anchor = anchor
 
     def sink_bytes(self) -> list[int]:
-        return [self.o.slot_row_byte(0, b) for b in range(2 * self.shape.layer_num)]
+        return [self.o.slot_row_byte(0, b) for b in range(self.geom.blocks)]
 
     def last_error(self) -> int:
         return gt.kv_pool_last_error(self.pool)
@@ -105,10 +106,14 @@ def assert_pool_matches(pp: PoolPair, M_prior: np.ndarray, tomb_rows: dict[int, 
         assert ok.all(), f"sink row of block {b} holds words from no candidate"
 
 
-def tomb_inputs(slots: np.ndarray, K: np.ndarray, V: np.ndarray, layer: int, R: int) -> dict:
-    """Rows written to the sink by tombstoned tokens, keyed by block."""
+def tomb_inputs(slots: np.ndarray, K: np.ndarray, V: np.ndarray | None, layer: int, R: int) -> dict:
+    """Rows written to the sink by tombstoned tokens, keyed by block (an MLA
+    pool, V None, has one latent block per layer)."""
     idx = np.nonzero(np.asarray(slots) < 0)[0]
-    Kr, Vr = as_rows(K, R), as_rows(V, R)
+    Kr = as_rows(K, R)
+    if V is None:
+        return {layer: [Kr[i] for i in idx]}
+    Vr = as_rows(V, R)
     return {2 * layer: [Kr[i] for i in idx], 2 * layer + 1: [Vr[i] for i in idx]}
 
 

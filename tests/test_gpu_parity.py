@@ -423,3 +423,111 @@ def test_block_table_matches_oracle(shape):
     gt.kv_translate(pp.pool, to_dev(slots), ids, to_dev(v2p))
     assert np.array_equal(ids.cpu().numpy(), want[kk].astype(np.int64) * ps + offs)
     pp.close()
+
+
+MLA_SHAPES = [
+    (S(0, "mla-deepseek-like", 6, 1, 576, 2, 64, 10), 0),  # latent 512+64 bf16: R=1152 (general row path)
+    (S(0, "mla-r512", 5, 1, 256, 2, 16, 30), 32),          # R=512
+    (S(0, "mla-fp8-r64", 9, 1, 64, 1, 32, 24), 0),          # R=64
+]
+
+
+@pytest.mark.parametrize("shape,anchor", MLA_SHAPES, ids=[s.name for s, _ in MLA_SHAPES])
+def test_mla_path_matches_oracle(shape, anchor):
+    """MLA pools (one latent row per layer, L blocks per page, no V): translate,
+    per-layer and all-layer stores (id and fused forms), gathers and a move,
+    each against the oracle on the whole pool."""
+    rng = np.random.default_rng(500 + shape.row_bytes)
+    pp = PoolPair(shape, anchor, latent=True)
+    o, R, L = pp.o, pp.R, shape.layer_num
+    ps, P = shape.page_size, shape.num_pages
+    assert pp.pool.info["blocks_per_page"] == L and pp.pool.info["latent_only"] == 1
+    M0 = pp.M.copy()
+    tombs: dict = {}
+    stored = set()
+    for layer in sorted({0, L // 2, L - 1}):
+        slots = _tokens(shape, rng, 150, 5)
+        K = synth.kv_values(rng, (slots.size, shape.head_num, shape.head_dim), shape.itemsize)
+        err = o.store(pp.M, layer, slots, K, None)
+        ids_ref, _ = o.translate(slots)
+        ids = torch.empty(slots.size, dtype=torch.int32, device="cuda")
+        gt.kv_translate(pp.pool, to_dev(slots), ids)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        if layer == 0:
+            gt.kv_store_layer_slots(pp.pool, layer, to_dev(slots), to_dev(K), None)
+        else:
+            gt.kv_store_layer(pp.pool, layer, ids, to_dev(K), None)
+        assert pp.last_error() == dev_bits(err) == 0
+        tombs = merge(tombs, tomb_inputs(slots, K, None, layer, R))
+        stored.update(int(t) for t in slots if t >= 0)
+        assert_pool_matches(pp, M0, tombs)
+    slots = _tokens(shape, rng, 120, 2)
+    Ka = synth.kv_values(rng, (L, slots.size, shape.head_num, shape.head_dim), shape.itemsize)
+    err = o.store_all(pp.M, slots, Ka, None)
+    ids = torch.empty(slots.size, dtype=torch.int32, device="cuda")
+    gt.kv_translate(pp.pool, to_dev(slots), ids)
+    gt.kv_store_all_layers(pp.pool, ids, to_dev(Ka), None)
+    assert pp.last_error() == dev_bits(err) == 0
+    for layer in range(L):
+        tombs = merge(tombs, tomb_inputs(slots, Ka[layer], None, layer, R))
+    stored.update(int(t) for t in slots if t >= 0)
+    assert_pool_matches(pp, M0, tombs)
+    # gathers: latent rows only
+    S_, maxp = 7, min(P - 1, 5)
+    bt = np.stack([1 + rng.permutation(P - 1)[:maxp] for _ in range(S_)]).astype(np.int32)
+    ln = rng.integers(0, maxp * ps + 1, size=S_).astype(np.int32)
+    st = np.minimum(rng.integers(0, ps + 3, size=S_), ln).astype(np.int32)
+    gb = synth.GatherBatch(bt, st, ln)
+    for layer in sorted({0, L - 1}):
+        rows = gb.total + 3
+        ok = np.full((rows, R), 0x33, np.uint8)
+        ok, ov, err = o.gather(pp.M, layer, bt, ln, gb.cu, st, rows, ok, None)
+        dk = torch.full((rows, R), 0x33, dtype=torch.uint8, device="cuda")
+        gt.kv_gather_layer(pp.pool, layer, to_dev(bt), to_dev(ln), to_dev(gb.cu), dk, None, to_dev(st))
+        assert err == 0 and pp.last_error() == 0
+        assert_bytes_equal(dk.cpu().numpy(), ok, f"MLA gather layer {layer}", R)
+    # move: all L latent rows of stored tokens to free tokens
+    free = np.setdiff1d(np.arange(ps, P * ps, dtype=np.int64), np.array(sorted(stored), np.int64))
+    m = min(40, len(stored), free.size)
+    src_slots = rng.choice(sorted(stored), size=m, replace=False).astype(np.int64)
+    dst_slots = rng.choice(free, size=m, replace=False).astype(np.int64)
+    si, _ = o.translate(src_slots)
+    di, _ = o.translate(dst_slots)
+    err = o.move(pp.M, si, di)
+    gt.kv_move(pp.pool, to_dev(si), to_dev(di))
+    assert err == 0 and pp.last_error() == 0
+    assert_pool_matches(pp, M0, tombs)
+    # an MHA-only argument error stays an error on an MHA pool
+    mha = PoolPair(synth.SHAPES[1], mirror=False)
+    with pytest.raises(gt.KVError):
+        gt.kv_store_layer(mha.pool, 0, ids[:4], to_dev(np.zeros((4, mha.R), np.uint8)), None)
+    mha.close()
+    pp.close()
+
+
+def test_library_owned_buffer_round_trip():
+    """kv_pool_create without a buffer: the library allocates anchor + total +
+    tail pad bytes itself; a store then a gather returns the stored rows, and
+    kv_pool_destroy frees it."""
+    shape = synth.SHAPES[2].scaled(20)
+    ps, P = shape.page_size, shape.num_pages
+    desc = gt.make_desc(shape.layer_num, shape.head_num, shape.head_dim, shape.itemsize, ps, P, anchor_bytes=256)
+    pool = gt.kv_pool_create(desc)
+    info = pool.info
+    total, pad = gt.kv_pool_required_bytes(desc)
+    assert info["owns_raw"] == 1 and info["raw_dev"] and info["raw_bytes"] == 256 + total + pad
+    rng = np.random.default_rng(21)
+    pages = (1 + rng.permutation(P - 1)[:4]).astype(np.int32)
+    slots = (pages.astype(np.int64)[:, None] * ps + np.arange(ps)).reshape(-1)
+    K, V = _vals(shape, rng, (slots.size,))
+    ids = torch.empty(slots.size, dtype=torch.int32, device="cuda")
+    gt.kv_translate(pool, to_dev(slots), ids)
+    gt.kv_store_layer(pool, 5, ids, to_dev(K), to_dev(V))
+    g = synth.GatherBatch(pages[None, :], np.zeros(1, np.int32), np.array([slots.size], np.int32))
+    dk = torch.empty((g.total, shape.row_bytes), dtype=torch.uint8, device="cuda")
+    dv = torch.empty_like(dk)
+    gt.kv_gather_layer(pool, 5, to_dev(g.block_table), to_dev(g.seq_len), to_dev(g.cu), dk, dv)
+    assert gt.kv_pool_last_error(pool) == 0
+    assert np.array_equal(dk.cpu().numpy(), as_rows(K, shape.row_bytes))
+    assert np.array_equal(dv.cpu().numpy(), as_rows(V, shape.row_bytes))
+    gt.kv_pool_destroy(pool)

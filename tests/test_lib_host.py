@@ -52,6 +52,13 @@ GATES = [
      "anchor"),
     (dict(layer_num=2, head_num=0, head_dim=8, itemsize=2, page_size=4, num_pages=64), -1, "bad_arg"),
     (dict(layer_num=2, head_num=2, head_dim=8, itemsize=2, page_size=0, num_pages=64), -1, "bad_arg"),
+    # MLA: one latent row per layer, asymmetric head dims admitted, bound over L blocks
+    (dict(layer_num=2, head_num=1, head_dim=16, itemsize=2, page_size=4, num_pages=64, v_head_dim=128,
+          latent_only=True), 0, "ok"),
+    (dict(layer_num=61, head_num=1, head_dim=576, itemsize=2, page_size=64, num_pages=550072, latent_only=True), 0,
+     "ok"),
+    (dict(layer_num=61, head_num=1, head_dim=576, itemsize=2, page_size=64, num_pages=550073, latent_only=True), -3,
+     "id_bound"),
 ]
 
 
@@ -61,7 +68,7 @@ def test_gates_agree_with_oracle(lib, kw, code, verdict):
     rc = lib.kv_pool_required_bytes(ctypes.byref(d), None, None)
     assert rc == code, gt.STATUS.get(rc)
     g = oracle.Geometry(kw["layer_num"], kw["head_num"], kw["head_dim"], kw["itemsize"], kw["page_size"],
-                        kw["num_pages"], kw.get("anchor_bytes", 0), kw.get("v_head_dim"))
+                        kw["num_pages"], kw.get("anchor_bytes", 0), kw.get("v_head_dim"), kw.get("latent_only", False))
     assert oracle.Oracle(g).check() == verdict
 
 
@@ -92,3 +99,18 @@ def test_entry_points_reject_null_pool(lib):
     assert lib.kv_store_layer(None, 0, vp(16), 1, vp(16), vp(16), None) in (-1, -6)
     assert lib.kv_move(None, vp(16), vp(16), 1, None) in (-1, -6)
     assert lib.kv_pool_destroy(None) == 0
+
+
+def test_bulk_copy_gather_variant_compiles(tmp_path):
+    """The cp.async.bulk form of the gather (a compile-time alternative to the
+    vector-copy kernel) stays buildable for sm_103a."""
+    import subprocess
+
+    from gather_translate_kv_gb300 import build
+
+    src = build.os.path.join(build.CSRC, "kv_gather.cu")
+    out = tmp_path / "g.o"
+    cmd = [build.nvcc(), "-c", src, "-o", str(out)] + build.NVCC_FLAGS + \
+        ["-DGTKV_GATHER_BULK=1", "-DGTKV_BULK_WARPS=8", "-DGTKV_BULK_STAGES=2"]
+    subprocess.check_call(cmd)
+    assert out.exists()
