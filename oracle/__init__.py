@@ -125,6 +125,8 @@ def lib(path: str | None = None):
         L.ora_move_rows.restype = ctypes.c_int
         L.ora_block_table_kf.argtypes = [P(_Desc), vp, c32, c32, vp, vp, c64, vp]
         L.ora_block_table_kf.restype = ctypes.c_int
+        L.ora_translate_mapped.argtypes = [P(_Desc), vp, c64, vp, c64, vp, c64, vp]
+        L.ora_translate_mapped.restype = ctypes.c_int
         if path is not None:
             return L
         _lib = L
@@ -170,6 +172,16 @@ class Oracle:
         err = self._L.ora_translate(
             ctypes.byref(self._d), _ptr(slots), slots.size, _ptr(v), 0 if v is None else v.size, _ptr(ids)
         )
+        return ids, err
+
+    def translate_mapped(self, slots: np.ndarray, tmap: np.ndarray, v2p: np.ndarray | None = None):
+        """Full-pool slots -> this (SWA) pool's ids through a token map."""
+        slots = np.ascontiguousarray(slots, dtype=np.int64)
+        tm = np.ascontiguousarray(tmap, dtype=np.int64)
+        ids = np.empty(slots.shape, dtype=np.int32)
+        v = None if v2p is None else np.ascontiguousarray(v2p, dtype=np.int32)
+        err = self._L.ora_translate_mapped(ctypes.byref(self._d), _ptr(slots), slots.size, _ptr(tm), tm.size,
+                                           _ptr(v), 0 if v is None else v.size, _ptr(ids))
         return ids, err
 
     def slot_row_byte(self, slot: int, block: int, v2p: np.ndarray | None = None) -> int:

@@ -487,3 +487,33 @@ int ora_block_table_kf(const ora_desc* d, const int32_t* virt, int32_t n_seqs, i
     }
     return err;
 }
+
+/* ------------------------------------------------ full -> SWA token mapping */
+
+/* Translate through a token map first. A hybrid model keeps a full-attention
+ * sub-pool and a sliding-window sub-pool in the same dense id space (实现拆解
+ * step 2: init_unified_swa_pools moves into the new id space) and addresses a
+ * token of an SWA layer through the full -> SWA token mapping, whose cleared
+ * entries are tombstones (功能与动机 / 关联脉络: clear_full_to_swa_mapping, PR
+ * #35773). Reading taken: slot t of the full pool becomes t' = tmap[t]; t < 0
+ * or t' < 0 is a tombstone (id 0, the sink); t >= tmap_len raises ORA_E_V2P
+ * and gives id 0; t' then goes through ora_translate's page logic (with the
+ * SWA pool's optional page map). */
+int ora_translate_mapped(const ora_desc* d, const int64_t* slots, int64_t n, const int64_t* tmap,
+                         int64_t tmap_len, const int32_t* v2p, int64_t v2p_len, int32_t* ids) {
+    int err = 0;
+    int64_t stride = (int64_t)d->page_size * blocks_of(d);
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = slots[i];
+        int64_t mapped = -1;
+        if (t >= 0) {
+            if (t >= tmap_len) err |= ORA_E_V2P;
+            else mapped = tmap[t];
+        }
+        int64_t p, o;
+        int sink;
+        err |= locate_slot(d, mapped, v2p, v2p_len, &p, &o, &sink);
+        ids[i] = (int32_t)(p * stride + o);
+    }
+    return err;
+}

@@ -446,10 +446,31 @@ def pin_mla(so):
     assert np.array_equal(M, T)
 
 
+def pin_swa_token_map(so):
+    """Full -> SWA token mapping (tests/golden/swa_map_tiny.txt), a slot past
+    the map, and translate_mapped(t) = translate(map[t]) on random maps."""
+    o = _mk(so, _geom(2, 1, 16, 1, 4, 16))
+    tmap = np.array([-1, 5, 6, -1, 17, 18, 19, 40, 63, 0, -1, 22], np.int64)
+    rows = _rows(os.path.join(GOLDEN, "swa_map_tiny.txt"))
+    slots = np.array([int(r[0]) for r in rows], np.int64)
+    want = np.array([int(r[1]) for r in rows], np.int32)
+    ids, err = o.translate_mapped(slots, tmap)
+    assert err == 0 and np.array_equal(ids, want), ids
+    ids, err = o.translate_mapped(np.array([12, 1], np.int64), tmap)
+    assert err == oracle.E_V2P and list(ids) == [0, 17]
+    rng = np.random.default_rng(18)
+    tm = rng.integers(-1, 64, size=200).astype(np.int64)
+    sl = rng.integers(-2, 200, size=500).astype(np.int64)
+    v2p = rng.permutation(16).astype(np.int32)
+    ids, err = o.translate_mapped(sl, tm, v2p)
+    ref, err2 = o.translate(np.where(sl < 0, -1, tm[np.clip(sl, 0, 199)]), v2p)
+    assert err == err2 == 0 and np.array_equal(ids, ref)
+
+
 PINS = [
     pin_translate_golden, pin_layout_table, pin_gates, pin_bijection, pin_store_vs_strided,
     pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors, pin_address_mode,
-    pin_block_table_kf, pin_mla,
+    pin_block_table_kf, pin_mla, pin_swa_token_map,
 ]
 
 

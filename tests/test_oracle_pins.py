@@ -25,8 +25,8 @@ def test_pin_holds(pin, oracle_lib):
 # (name, original text, planted mistake)
 MUTANTS = [
     ("stride_drops_factor_2",
-     "int64_t stride = (int64_t)d->page_size * blocks_of(d);\n    for",
-     "int64_t stride = (int64_t)d->page_size * (int64_t)d->layer_num;\n    for"),
+     "int64_t stride = (int64_t)d->page_size * blocks_of(d);\n    for (int64_t i = 0; i < n; ++i) {\n        int64_t p, o;",
+     "int64_t stride = (int64_t)d->page_size * (int64_t)d->layer_num;\n    for (int64_t i = 0; i < n; ++i) {\n        int64_t p, o;"),
     ("mha_blocks_per_page_L",
      "return d->latent_only ? (int64_t)d->layer_num : 2 * (int64_t)d->layer_num;",
      "return d->latent_only ? (int64_t)d->layer_num : (int64_t)d->layer_num;"),
@@ -84,6 +84,9 @@ MUTANTS = [
     ("block_table_prefix_floor",
      "int64_t np = len > 0 ? (len + ps - 1) / ps : 0;",
      "int64_t np = len > 0 ? len / ps : 0;"),
+    ("swa_map_skipped",
+     "            else mapped = tmap[t];",
+     "            else mapped = t;"),
     ("asymmetric_not_rejected",
      "if (!d->latent_only && d->head_dim != d->v_head_dim) return ORA_ASYMMETRIC;",
      ""),
