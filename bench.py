@@ -494,7 +494,7 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ per-kernel table
 
-MICRO_DEFAULT = ["translate:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2", "move:2",
+MICRO_DEFAULT = ["translate:2", "block_table:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2", "move:2",
                  "translate:3", "store:3", "store_slots:3", "store_all:3", "gather:3",
                  "store:4", "gather:4", "move:4",
                  "translate:5", "store:5", "store_slots:5", "gather:5", "move:5",
@@ -618,6 +618,16 @@ def run_micro(args):
         if "translate" in kernels:
             ms = timed(lambda i: gt.kv_translate(pool, slots_d, ids), calls, True)
             report("translate", cfg, f"{n} slots", ms, n * 12, n)
+        if "block_table" in kernels:
+            gbt = synth.gather_batch(sh)
+            vt = d(gbt.block_table)
+            vmap = d(np.random.default_rng(3).permutation(P).astype(np.int32))
+            kf = torch.empty_like(vt)
+            lnt = d(gbt.seq_len)
+            ne = gbt.block_table.size
+            ms = timed(lambda i: gt.kv_translate_block_table(pool, vt, lnt, vmap, kf), calls, True)
+            report("translate_block_table", cfg, f"{gbt.block_table.shape[0]} x {gbt.block_table.shape[1]} entries",
+                   ms, ne * 12, ne)
         if "store" in kernels or "store_graph" in kernels or "store_slots" in kernels:
             K = _payload_torch(gen, n, R, sh.itemsize, dev)
             V = None if sh.latent else _payload_torch(gen, n, R, sh.itemsize, dev)

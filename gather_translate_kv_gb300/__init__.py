@@ -106,6 +106,7 @@ def lib():
         "kv_pool_destroy": [vp],
         "kv_pool_info": [vp, P(kv_pool_info_t)],
         "kv_translate": [vp, vp, i64, vp, i64, vp, vp],
+        "kv_translate_mapped": [vp, vp, i64, vp, i64, vp, i64, vp, vp],
         "kv_store_layer": [vp, i32, vp, i64, vp, vp, vp],
         "kv_store_all_layers": [vp, vp, i64, vp, vp, vp],
         "kv_store_layer_slots": [vp, i32, vp, i64, vp, i64, vp, vp, vp],
@@ -217,6 +218,19 @@ def kv_translate(pool: KVPool, slots: torch.Tensor, ids_out: torch.Tensor, v2p: 
     _check("kv_translate", lib().kv_translate(
         pool.handle, _dev(slots, "slots", torch.int64), n, _dev(v2p, "v2p", torch.int32),
         0 if v2p is None else v2p.numel(), _dev(ids_out, "ids_out", torch.int32), _stream(stream)))
+    return ids_out
+
+
+def kv_translate_mapped(pool: KVPool, slots: torch.Tensor, ids_out: torch.Tensor, tmap: torch.Tensor,
+                        v2p: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Full-pool slots -> this (SWA) pool's ids through a full -> SWA token map."""
+    n = slots.numel()
+    if ids_out.numel() != n:
+        raise ValueError("ids_out must have one entry per slot")
+    _check("kv_translate_mapped", lib().kv_translate_mapped(
+        pool.handle, _dev(slots, "slots", torch.int64), n, _dev(tmap, "tmap", torch.int64), tmap.numel(),
+        _dev(v2p, "v2p", torch.int32), 0 if v2p is None else v2p.numel(), _dev(ids_out, "ids_out", torch.int32),
+        _stream(stream)))
     return ids_out
 
 

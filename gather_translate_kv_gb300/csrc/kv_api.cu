@@ -6,7 +6,7 @@
 
 #include <new>
 
-#include "kv_common.cuh"
+#include "kv_launch.h"
 #include "kv_layout.h"
 #include "kv_pool.h"
 
@@ -202,6 +202,26 @@ int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n
     return KV_ERR_ALIGN;
   return launched(gtkv::launch_store(pool->dev, 0, pool->desc.layer_num, ids_dev, n, k_all_dev, v_all_dev,
                                      pool->sm_count, as_stream(stream)));
+}
+
+int kv_translate_mapped(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int64_t* tmap_dev,
+                        int64_t tmap_len, const int32_t* v2p_dev, int64_t v2p_len, int32_t* ids_dev,
+                        kv_stream_t stream) {
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  if (n < 0 || tmap_len < 0 || v2p_len < 0) return KV_ERR_INVALID;
+  if (n == 0) return KV_OK;
+  if (slots_dev == nullptr || ids_dev == nullptr || (tmap_dev == nullptr && tmap_len > 0) ||
+      (v2p_dev == nullptr && v2p_len > 0))
+    return KV_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(slots_dev) & 7u) || (reinterpret_cast<uintptr_t>(tmap_dev) & 7u) ||
+      (reinterpret_cast<uintptr_t>(ids_dev) & 3u) || (reinterpret_cast<uintptr_t>(v2p_dev) & 3u))
+    return KV_ERR_ALIGN;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(slots_dev), s1 = s0 + 8 * static_cast<uintptr_t>(n);
+  const uintptr_t i0 = reinterpret_cast<uintptr_t>(ids_dev), i1 = i0 + 4 * static_cast<uintptr_t>(n);
+  if (i0 < s1 && s0 < i1) return KV_ERR_INVALID;
+  return launched(gtkv::launch_translate_mapped(pool->dev, slots_dev, n, tmap_dev, tmap_len, v2p_dev, v2p_len, ids_dev,
+                                                pool->sm_count, as_stream(stream)));
 }
 
 static int store_slots(const kv_pool_t* pool, int32_t layer0, int32_t n_layers, const int64_t* slots_dev, int64_t n,

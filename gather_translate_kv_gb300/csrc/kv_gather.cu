@@ -17,7 +17,7 @@
 // and V bytes as 16-byte vectors, all loads issued before the stores. No
 // search and no host synchronization: the item space is n_seqs x max_pages x
 // chunks_per_page, and an entry outside a sequence's window is an empty item.
-#include "kv_common.cuh"
+#include "kv_launch.h"
 
 namespace gtkv {
 

@@ -8,7 +8,7 @@
 // tasks, so the 2L rows of a pair are spread over consecutive row groups.
 // Sources and destinations are disjoint by precondition, so loads use the
 // coherent path (the pool is written by this kernel) and need no ordering.
-#include "kv_common.cuh"
+#include "kv_launch.h"
 
 namespace gtkv {
 

@@ -10,7 +10,7 @@
 // (contiguous K/V inputs) and 2 rows out (scattered pool rows). In an MLA pool
 // (one latent row per layer, blocks_per_page = L) the row is id + l*ps and
 // there is no V.
-#include "kv_common.cuh"
+#include "kv_launch.h"
 
 namespace gtkv {
 

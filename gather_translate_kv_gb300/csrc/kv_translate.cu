@@ -3,7 +3,7 @@
 // multi_ended_allocator.py, translate_kv_loc_for_kernel: split slots into
 // pages and offsets, map pages virtual -> physical, scale by the page stride
 // ps * 2L and clamp tombstones to 0 (the page-0 sink).
-#include "kv_common.cuh"
+#include "kv_launch.h"
 
 namespace gtkv {
 
@@ -64,7 +64,39 @@ __global__ void __launch_bounds__(kBlock) k_block_table(DevPool p, const int32_t
   if (bits) atomicOr(p.err, bits);
 }
 
+// Full -> SWA token map, then translate (one slot per thread): t' = tmap[t]
+// for 0 <= t < tmap_len (a negative t' is a cleared entry: the sink), t < 0
+// is a tombstone, t >= tmap_len an error that also gives the sink.
+__global__ void __launch_bounds__(kBlock) k_translate_mapped(DevPool p, const int64_t* __restrict__ slots, int64_t n,
+                                                             const int64_t* __restrict__ tmap, int64_t tmap_len,
+                                                             const int32_t* __restrict__ v2p, int64_t v2p_len,
+                                                             int32_t* __restrict__ ids) {
+  int bits = 0;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += step) {
+    const int64_t t = __ldg(slots + i);
+    int64_t mapped = -1;
+    if (t >= 0) {
+      if (t < tmap_len) {
+        mapped = __ldg(tmap + t);
+      } else {
+        bits |= KV_DEV_ERR_V2P;
+      }
+    }
+    ids[i] = static_cast<int32_t>(slot_to_id(p, mapped, v2p, v2p_len, bits));
+  }
+  if (bits) atomicOr(p.err, bits);
+}
+
 }  // namespace
+
+cudaError_t launch_translate_mapped(const DevPool& p, const int64_t* slots, int64_t n, const int64_t* tmap,
+                                    int64_t tmap_len, const int32_t* v2p, int64_t v2p_len, int32_t* ids, int sm_count,
+                                    cudaStream_t s) {
+  const unsigned grid = grid_for(k_translate_mapped, (n + 31) / 32, sm_count);
+  k_translate_mapped<<<grid, kBlock, 0, s>>>(p, slots, n, tmap, tmap_len, v2p, v2p_len, ids);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_block_table(const DevPool& p, const int32_t* virt, int32_t n_seqs, int32_t max_pages,
                                const int32_t* seq_len, const int32_t* v2p, int64_t v2p_len, int32_t* out,

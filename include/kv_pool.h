@@ -168,6 +168,23 @@ int kv_pool_info(const kv_pool_t* pool, kv_pool_info_t* out);
 int kv_translate(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int32_t* v2p_dev,
                  int64_t v2p_len, int32_t* ids_dev, kv_stream_t stream);
 
+/* Full -> SWA token mapping, then translate: for slot t of the full-attention
+ * sub-pool, t' = tmap[t] is the token's slot in this (sliding-window)
+ * sub-pool, and ids[i] is kv_translate of t' (with the optional page map).
+ * Source: SWA sub-pools share the dense id space (实现拆解 step 2,
+ * init_unified_swa_pools) and are addressed through the full -> SWA token
+ * mapping, whose cleared entries are tombstones (关联脉络: PR #35773,
+ * clear_full_to_swa_mapping).
+ *  slots_dev  int64 [n] full-pool slots (negative = tombstone)
+ *  tmap_dev   int64 [tmap_len] full slot -> SWA slot (negative = cleared)
+ *  v2p_dev    int32 [v2p_len] page map of this pool, or NULL
+ *  ids_dev    int32 [n] output; must not overlap slots_dev
+ * A tombstone or cleared entry gives id 0 (the sink). Device errors: a slot
+ * >= tmap_len sets KV_DEV_ERR_V2P (id 0); then as kv_translate. */
+int kv_translate_mapped(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int64_t* tmap_dev,
+                        int64_t tmap_len, const int32_t* v2p_dev, int64_t v2p_len, int32_t* ids_dev,
+                        kv_stream_t stream);
+
 /* Per-layer store: row i of K goes to block 2*layer and row i of V to block
  * 2*layer+1 of token ids_dev[i], i.e. bytes anchor + (id + 2*layer*ps) * R and
  * anchor + (id + (2*layer+1)*ps) * R.
