@@ -27,6 +27,81 @@ namespace {
 #define GTKV_GATHER_CHUNK 4096  // bytes of K (and of V) one warp copies per item
 #endif
 
+// Metadata checks, one sequence per thread, grid-stride (they never gate the
+// copies: every access is bounds-checked on its own): KV_DEV_ERR_TABLE when
+// start < 0, len > max_pages * ps, cu_out not non-decreasing from 0 or a span
+// shorter than its tokens, or cu_out[n_seqs] > out_rows.
+__device__ __forceinline__ void check_gather_meta(const DevPool& p, int32_t n_seqs, int32_t max_pages,
+                                                  const int32_t* __restrict__ seq_start,
+                                                  const int32_t* __restrict__ seq_len,
+                                                  const int64_t* __restrict__ cu, int64_t out_rows, int64_t tid,
+                                                  int64_t nthreads) {
+  for (int64_t s = tid; s < n_seqs; s += nthreads) {
+    const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
+    const int64_t b = __ldg(seq_len + s);
+    const int64_t c0 = __ldg(cu + s), c1 = __ldg(cu + s + 1);
+    if (a < 0 || b > static_cast<int64_t>(max_pages) * p.ps || c0 < 0 || c1 < c0 || c1 - c0 < b - a)
+      atomicOr(p.err, KV_DEV_ERR_TABLE);
+  }
+  if (tid == 0 && __ldg(cu + n_seqs) > out_rows) atomicOr(p.err, KV_DEV_ERR_TABLE);
+}
+
+// One work item: chunk c of block-table entry (s, k), clipped to the window
+// [start_s, len_s), to tokens >= 0 and to output rows [0, out_rows).
+struct Run {
+  int64_t src;   // 16-byte vector index (from p.base) of its first K row; V is ps rows later
+  int64_t row;   // first output row
+  int64_t nvec;  // 16-byte vectors of K (and of V)
+  int kind;      // 0: nothing to copy; 1: rows of a page; 2: tombstoned entry, every row reads the sink
+};
+
+__device__ __forceinline__ Run gather_item(const DevPool& p, int64_t it, int64_t koff, const int32_t* __restrict__ bt,
+                                           int32_t max_pages, const int32_t* __restrict__ seq_start,
+                                           const int32_t* __restrict__ seq_len, const int64_t* __restrict__ cu,
+                                           int64_t out_rows, int32_t chunk_rows, int32_t chunks_per_page,
+                                           bool report) {
+  Run r{0, 0, 0, 0};
+  const int64_t ps = p.ps;
+  const int64_t sk = it / chunks_per_page;  // block-table entry index s*max_pages + k
+  const int64_t c = it - sk * chunks_per_page;
+  const int64_t s = sk / max_pages;
+  const int64_t k = sk - s * max_pages;
+  const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
+  const int64_t b = __ldg(seq_len + s);
+  const int64_t j0 = k * ps + c * chunk_rows;  // first token of this chunk
+  int64_t jlo = j0 > a ? j0 : a;
+  if (jlo < 0) jlo = 0;
+  int64_t jhi = j0 + chunk_rows;
+  if (jhi > (k + 1) * ps) jhi = (k + 1) * ps;
+  if (jhi > b) jhi = b;
+  if (jlo >= jhi) return r;  // entry outside the window: empty item
+  const int64_t page = __ldg(bt + sk);
+  if (page >= p.num_pages) {
+    if (report) atomicOr(p.err, KV_DEV_ERR_ROW);
+    return r;
+  }
+  const int64_t cs = __ldg(cu + s);
+  int64_t rlo = cs + (jlo - a);
+  int64_t rhi = cs + (jhi - a);
+  if (rlo < 0) {  // rows before 0 are never written (cu_out[s] < 0 is flagged)
+    jlo -= rlo;
+    rlo = 0;
+  }
+  if (rhi > out_rows) rhi = out_rows;
+  if (rlo >= rhi) return r;
+  r.row = rlo;
+  r.nvec = (rhi - rlo) * p.vpr;
+  if (page < 0) {
+    r.kind = 2;
+    r.src = koff * p.vpr;
+  } else {
+    r.kind = 1;
+    r.src = (page * p.stride + koff + (jlo - k * ps)) * p.vpr;
+  }
+  return r;
+}
+
+
 // Items = (sequence s, table entry k, chunk c). CHV 16-byte vectors per lane
 // per round: one round moves 32*CHV vectors of K and as many of V.
 template <int CHV>
@@ -39,66 +114,31 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
                                                         int32_t chunk_rows, int32_t chunks_per_page) {
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t ps = p.ps;
-
-  // Metadata checks, one sequence per thread (they never gate the copies:
-  // every access below is bounds-checked on its own).
-  for (int64_t s = tid; s < n_seqs; s += nthreads) {
-    const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
-    const int64_t b = __ldg(seq_len + s);
-    const int64_t c0 = __ldg(cu + s), c1 = __ldg(cu + s + 1);
-    if (a < 0 || b > static_cast<int64_t>(max_pages) * ps || c0 < 0 || c1 < c0 || c1 - c0 < b - a)
-      atomicOr(p.err, KV_DEV_ERR_TABLE);
-  }
-  if (tid == 0 && __ldg(cu + n_seqs) > out_rows) atomicOr(p.err, KV_DEV_ERR_TABLE);
+  check_gather_meta(p, n_seqs, max_pages, seq_start, seq_len, cu, out_rows, tid, nthreads);
 
   const int lane = threadIdx.x & 31;
   const int64_t vpr = p.vpr;
-  const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * ps;  // K (or latent) block of the layer
+  const int64_t ps_vec = p.ps * vpr;                                      // K -> V distance, in vectors
+  const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * p.ps;  // K (or latent) block of the layer
   const bool has_v = p.kv_rows == 2;
   const int64_t n_items = static_cast<int64_t>(n_seqs) * max_pages * chunks_per_page;
   const L2Policy pol = make_l2_policy();
 
   for (int64_t it = tid >> 5; it < n_items; it += nthreads >> 5) {
-    const int64_t sk = it / chunks_per_page;  // block-table entry index s*max_pages + k
-    const int64_t c = it - sk * chunks_per_page;
-    const int64_t s = sk / max_pages;
-    const int64_t k = sk - s * max_pages;
-    const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
-    const int64_t b = __ldg(seq_len + s);
-    const int64_t j0 = k * ps + c * chunk_rows;  // first token of this chunk
-    int64_t jlo = j0 > a ? j0 : a;
-    if (jlo < 0) jlo = 0;
-    int64_t jhi = j0 + chunk_rows;
-    if (jhi > (k + 1) * ps) jhi = (k + 1) * ps;
-    if (jhi > b) jhi = b;
-    if (jlo >= jhi) continue;  // entry outside the window: empty item
-    int64_t page = __ldg(bt + sk);
-    if (page >= p.num_pages) {
-      if (lane == 0) atomicOr(p.err, KV_DEV_ERR_ROW);
-      continue;
-    }
-    const int64_t cs = __ldg(cu + s);
-    int64_t rlo = cs + (jlo - a);
-    int64_t rhi = cs + (jhi - a);
-    if (rlo < 0) {  // rows before 0 are never written (cu_out[s] < 0 is flagged)
-      jlo -= rlo;
-      rlo = 0;
-    }
-    if (rhi > out_rows) rhi = out_rows;
-    if (rlo >= rhi) continue;
-    const int64_t nvec = (rhi - rlo) * vpr;
-    uint4* dk = out_k + rlo * vpr;
-    uint4* dv = has_v ? out_v + rlo * vpr : nullptr;
-    if (page >= 0) {
-      const uint4* srck = p.base + (page * p.stride + koff + (jlo - k * ps)) * vpr;
-      const uint4* srcv = srck + ps * vpr;
-      for (int64_t v0 = 0; v0 < nvec; v0 += 32 * CHV) {
+    const Run r = gather_item(p, it, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows,
+                              chunks_per_page, lane == 0);
+    if (r.kind == 0) continue;
+    uint4* dk = out_k + r.row * vpr;
+    uint4* dv = has_v ? out_v + r.row * vpr : nullptr;
+    const uint4* srck = p.base + r.src;
+    const uint4* srcv = srck + ps_vec;
+    if (r.kind == 1) {
+      for (int64_t v0 = 0; v0 < r.nvec; v0 += 32 * CHV) {
         uint4 bk[CHV], bv[CHV];
 #pragma unroll
         for (int i = 0; i < CHV; ++i) {
           const int64_t v = v0 + lane + 32 * i;
-          if (v < nvec) {
+          if (v < r.nvec) {
             bk[i] = ld16<GTKV_GATHER_LD>(srck + v, pol);
             if (has_v) bv[i] = ld16<GTKV_GATHER_LD>(srcv + v, pol);
           }
@@ -106,16 +146,14 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
 #pragma unroll
         for (int i = 0; i < CHV; ++i) {
           const int64_t v = v0 + lane + 32 * i;
-          if (v < nvec) {
+          if (v < r.nvec) {
             st16<GTKV_GATHER_ST>(dk + v, bk[i], pol);
             if (has_v) st16<GTKV_GATHER_ST>(dv + v, bv[i], pol);
           }
         }
       }
     } else {  // tombstoned entry: every token of the run reads the page-0 sink row
-      const uint4* srck = p.base + koff * vpr;
-      const uint4* srcv = srck + ps * vpr;
-      for (int64_t v = lane; v < nvec; v += 32) {
+      for (int64_t v = lane; v < r.nvec; v += 32) {
         const int64_t col = v % vpr;
         st16<GTKV_GATHER_ST>(dk + v, ld16<GTKV_GATHER_LD>(srck + col, pol), pol);
         if (has_v) st16<GTKV_GATHER_ST>(dv + v, ld16<GTKV_GATHER_LD>(srcv + col, pol), pol);
@@ -199,14 +237,7 @@ __global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t ps = p.ps;
-  for (int64_t s = tid; s < n_seqs; s += nthreads) {
-    const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
-    const int64_t b = __ldg(seq_len + s);
-    const int64_t c0 = __ldg(cu + s), c1 = __ldg(cu + s + 1);
-    if (a < 0 || b > static_cast<int64_t>(max_pages) * ps || c0 < 0 || c1 < c0 || c1 - c0 < b - a)
-      atomicOr(p.err, KV_DEV_ERR_TABLE);
-  }
-  if (tid == 0 && __ldg(cu + n_seqs) > out_rows) atomicOr(p.err, KV_DEV_ERR_TABLE);
+  check_gather_meta(p, n_seqs, max_pages, seq_start, seq_len, cu, out_rows, tid, nthreads);
 
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
@@ -269,42 +300,13 @@ __global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
     uint32_t bytes = 0;
     bool sink = false;
     if (it < n_items) {
-      const int64_t sk = it / chunks_per_page;
-      const int64_t c = it - sk * chunks_per_page;
-      const int64_t s = sk / max_pages;
-      const int64_t k = sk - s * max_pages;
-      const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
-      const int64_t b = __ldg(seq_len + s);
-      const int64_t j0 = k * ps + c * chunk_rows;
-      int64_t jlo = j0 > a ? j0 : a;
-      if (jlo < 0) jlo = 0;
-      int64_t jhi = j0 + chunk_rows;
-      if (jhi > (k + 1) * ps) jhi = (k + 1) * ps;
-      if (jhi > b) jhi = b;
-      if (jlo < jhi) {
-        const int64_t page = __ldg(bt + sk);
-        if (page >= p.num_pages) {
-          atomicOr(p.err, KV_DEV_ERR_ROW);
-        } else {
-          const int64_t cs = __ldg(cu + s);
-          int64_t rlo = cs + (jlo - a);
-          int64_t rhi = cs + (jhi - a);
-          if (rlo < 0) {
-            jlo -= rlo;
-            rlo = 0;
-          }
-          if (rhi > out_rows) rhi = out_rows;
-          if (rlo < rhi) {
-            row = rlo;
-            bytes = static_cast<uint32_t>((rhi - rlo) * vpr * 16);
-            if (page < 0) {
-              sink = true;
-              src = koff * vpr;
-            } else {
-              src = (page * p.stride + koff + (jlo - k * ps)) * vpr;
-            }
-          }
-        }
+      const Run r = gather_item(p, it, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows,
+                                chunks_per_page, true);
+      if (r.kind != 0) {
+        src = r.src;
+        row = r.row;
+        bytes = static_cast<uint32_t>(r.nvec * 16);
+        sink = r.kind == 2;
       }
     }
     unsigned todo = __ballot_sync(kFull, src >= 0);

@@ -16,6 +16,30 @@ namespace gtkv {
 
 namespace {
 
+// The two halves of copy_rows for callers that can issue their loads before
+// the destinations are known (fixed-size rows only, VPL > 0).
+template <int G, int VPL, int N, int LD>
+__device__ __forceinline__ void load_rows(uint4 (&buf)[N][VPL], const uint4* const (&src)[N], const bool (&go)[N],
+                                          int g, const L2Policy& pol) {
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (go[i]) {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) buf[i][v] = ld16<LD>(src[i] + g + v * G, pol);
+    }
+}
+
+template <int G, int VPL, int N, int ST>
+__device__ __forceinline__ void store_rows(uint4* const (&dst)[N], const uint4 (&buf)[N][VPL], const bool (&go)[N],
+                                           int g, const L2Policy& pol) {
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (go[i]) {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) st16<ST>(dst[i] + g + v * G, buf[i][v], pol);
+    }
+}
+
 // Tasks t in [0, n_tasks), n_tasks = n_layers * n: layer = layer0 + t / n,
 // token i = t % n; the input rows are K[t] and V[t] (a [n_layers, n, H, D]
 // layout, n_layers = 1 for the per-layer call). A warp takes 32 consecutive
@@ -62,41 +86,71 @@ __global__ void __launch_bounds__(kBlock) k_store(DevPool p, int32_t layer0, int
   fetch(mine ? t0 + lane : n_tasks);
   for (; t0 < n_tasks; t0 += step) {
     const int64_t t = mine ? t0 + lane : n_tasks;
-    int64_t id = id_next;
+    const int64_t id_raw = id_next;
     const int64_t l = l_next;
     fetch(mine ? t0 + step + lane : n_tasks);  // next batch's ids, in flight during this batch's copies
-    if constexpr (SLOTS) {
-      if (t < n_tasks) id = slot_to_id(p, id, v2p, v2p_len, bits);
-    }
-    long long row = -1;  // K row of this lane's task, in view units; -1 = skip
-    if (t < n_tasks) {
-      if (id >= 0 && id < p.n_rows) {
-        row = id + (layer0 + l) * p.kv_rows * p.ps;
-      } else {
-        atomicOr(p.err, KV_DEV_ERR_ROW);
+    // K row of this lane's task in view units (-1 = skip); worked out after
+    // the first wave's data loads are issued, so a batch whose ids are still
+    // in flight overlaps the two loads
+    long long row = -1;
+    auto resolve = [&]() {
+      int64_t id = id_raw;
+      if constexpr (SLOTS) {
+        if (t < n_tasks) id = slot_to_id(p, id, v2p, v2p_len, bits);
       }
-    }
+      if (t < n_tasks) {
+        if (id >= 0 && id < p.n_rows) {
+          row = id + (layer0 + l) * p.kv_rows * p.ps;
+        } else {
+          atomicOr(p.err, KV_DEV_ERR_ROW);
+        }
+      }
+    };
     const int cnt = static_cast<int>(n_tasks - t0 < batch ? n_tasks - t0 : batch);
 #pragma unroll 1
     for (int w0 = 0; w0 < cnt; w0 += RPW * U) {
       const uint4* src[2 * U];
       uint4* dst[2 * U];
       bool go[2 * U];
+      bool ld[2 * U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = w0 + u * RPW + grp;  // task within the batch
-        const long long rr = __shfl_sync(kFull, row, j & 31);
-        const bool ok = j < cnt && rr >= 0;
-        const int64_t tt = ok ? t0 + j : 0;
-        const int64_t r_ = ok ? rr : 0;
-        go[2 * u] = ok;
-        go[2 * u + 1] = ok && V != nullptr;  // an MLA pool has no V rows
+        const int64_t tt = j < cnt ? t0 + j : 0;
+        ld[2 * u] = j < cnt;
+        ld[2 * u + 1] = j < cnt && V != nullptr;  // an MLA pool has no V rows
         src[2 * u] = K + tt * vpr;
         src[2 * u + 1] = (V != nullptr ? V : K) + tt * vpr;
-        dst[2 * u] = p.base + r_ * vpr;
-        dst[2 * u + 1] = p.base + (r_ + p.ps) * vpr;
       }
-      copy_rows<G, VPL, 2 * U, GTKV_STORE_LD, GTKV_STORE_ST>(src, dst, go, g, vpr, pol);
+      if constexpr (VPL > 0) {
+        uint4 buf[2 * U][VPL];
+        load_rows<G, VPL, 2 * U, GTKV_STORE_LD>(buf, src, ld, g, pol);  // sources do not depend on the ids
+        if (w0 == 0) resolve();
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = w0 + u * RPW + grp;
+          const long long rr = __shfl_sync(kFull, row, j & 31);
+          const int64_t r_ = rr >= 0 ? rr : 0;
+          go[2 * u] = ld[2 * u] && rr >= 0;
+          go[2 * u + 1] = ld[2 * u + 1] && rr >= 0;
+          dst[2 * u] = p.base + r_ * vpr;
+          dst[2 * u + 1] = p.base + (r_ + p.ps) * vpr;
+        }
+        store_rows<G, VPL, 2 * U, GTKV_STORE_ST>(dst, buf, go, g, pol);
+      } else {
+        if (w0 == 0) resolve();
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = w0 + u * RPW + grp;
+          const long long rr = __shfl_sync(kFull, row, j & 31);
+          const int64_t r_ = rr >= 0 ? rr : 0;
+          go[2 * u] = ld[2 * u] && rr >= 0;
+          go[2 * u + 1] = ld[2 * u + 1] && rr >= 0;
+          dst[2 * u] = p.base + r_ * vpr;
+          dst[2 * u + 1] = p.base + (r_ + p.ps) * vpr;
+        }
+        copy_rows<G, VPL, 2 * U, GTKV_STORE_LD, GTKV_STORE_ST>(src, dst, go, g, vpr, pol);
+      }
     }
   }
   if constexpr (SLOTS) {

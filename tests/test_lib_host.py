@@ -114,3 +114,44 @@ def test_bulk_copy_gather_variant_compiles(tmp_path):
         ["-DGTKV_GATHER_BULK=1", "-DGTKV_BULK_WARPS=8", "-DGTKV_BULK_STAGES=2"]
     subprocess.check_call(cmd)
     assert out.exists()
+
+
+def c_abi_program(tmp_path, with_cuda: bool):
+    """Build tests/c_abi_roundtrip.c as a plain C99 program against libgtkv.so."""
+    import os
+    import subprocess
+
+    from gather_translate_kv_gb300 import build
+
+    lib_path = build.build()
+    exe = tmp_path / ("c_abi_gpu" if with_cuda else "c_abi_host")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c_abi_roundtrip.c")
+    cuda = "/usr/local/cuda"
+    cmd = ["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", build.INCLUDE, src, "-o", str(exe),
+           lib_path, f"-Wl,-rpath,{os.path.dirname(lib_path)}"]
+    if with_cuda:
+        cmd += ["-DWITH_CUDA", "-I", f"{cuda}/include", f"-L{cuda}/lib64", "-lcudart",
+                f"-Wl,-rpath,{cuda}/lib64"]
+    subprocess.check_call(cmd)
+    return str(exe)
+
+
+def test_c_abi_from_plain_c(tmp_path):
+    """The header compiles as C99 with -Werror, the library links from C, and
+    the host-side gates answer as documented (no GPU needed)."""
+    import subprocess
+
+    exe = c_abi_program(tmp_path, with_cuda=False)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "c abi: ok" in r.stdout
+
+
+@pytest.mark.gpu
+def test_c_abi_round_trip_on_gpu(tmp_path):
+    """translate -> store -> gather through the C ABI from a C program."""
+    import subprocess
+
+    exe = c_abi_program(tmp_path, with_cuda=True)
+    r = subprocess.run([exe, "gpu"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
