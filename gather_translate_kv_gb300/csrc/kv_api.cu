@@ -2,6 +2,7 @@
 // kernel launches. Nothing here touches K/V bytes; every step of the path runs
 // in the kernels of kv_translate.cu, kv_store.cu, kv_gather.cu and kv_move.cu.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <new>
@@ -25,6 +26,15 @@ struct kv_pool {
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// An NVTX range around one API call, so profilers show which entry point
+// enqueued which kernel (a no-op when no tool is attached).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
 
 int ps_shift_of(int64_t ps) {
   if ((ps & (ps - 1)) != 0) return -1;
@@ -161,6 +171,7 @@ int kv_pool_info(const kv_pool_t* pool, kv_pool_info_t* out) {
 
 int kv_translate(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int32_t* v2p_dev,
                  int64_t v2p_len, int32_t* ids_dev, kv_stream_t stream) {
+  Range nvtx("kv_translate");
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (n < 0 || v2p_len < 0) return KV_ERR_INVALID;
@@ -178,6 +189,7 @@ int kv_translate(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, con
 
 int kv_store_layer(const kv_pool_t* pool, int32_t layer, const int32_t* ids_dev, int64_t n, const void* k_dev,
                    const void* v_dev, kv_stream_t stream) {
+  Range nvtx("kv_store_layer");
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (n < 0 || layer < 0 || layer >= pool->desc.layer_num) return KV_ERR_INVALID;
@@ -191,6 +203,7 @@ int kv_store_layer(const kv_pool_t* pool, int32_t layer, const int32_t* ids_dev,
 
 int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n, const void* k_all_dev,
                         const void* v_all_dev, kv_stream_t stream) {
+  Range nvtx("kv_store_all_layers");
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (n < 0) return KV_ERR_INVALID;
@@ -207,6 +220,7 @@ int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n
 int kv_translate_mapped(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int64_t* tmap_dev,
                         int64_t tmap_len, const int32_t* v2p_dev, int64_t v2p_len, int32_t* ids_dev,
                         kv_stream_t stream) {
+  Range nvtx("kv_translate_mapped");
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (n < 0 || tmap_len < 0 || v2p_len < 0) return KV_ERR_INVALID;
@@ -245,12 +259,14 @@ static int store_slots(const kv_pool_t* pool, int32_t layer0, int32_t n_layers, 
 int kv_store_layer_slots(const kv_pool_t* pool, int32_t layer, const int64_t* slots_dev, int64_t n,
                          const int32_t* v2p_dev, int64_t v2p_len, const void* k_dev, const void* v_dev,
                          kv_stream_t stream) {
+  Range nvtx("kv_store_layer_slots");
   if (pool != nullptr && (layer < 0 || layer >= pool->desc.layer_num)) return KV_ERR_INVALID;
   return store_slots(pool, layer, 1, slots_dev, n, v2p_dev, v2p_len, k_dev, v_dev, stream);
 }
 
 int kv_store_all_layers_slots(const kv_pool_t* pool, const int64_t* slots_dev, int64_t n, const int32_t* v2p_dev,
                               int64_t v2p_len, const void* k_all_dev, const void* v_all_dev, kv_stream_t stream) {
+  Range nvtx("kv_store_all_layers_slots");
   if (pool == nullptr) return KV_ERR_INVALID;
   return store_slots(pool, 0, pool->desc.layer_num, slots_dev, n, v2p_dev, v2p_len, k_all_dev, v_all_dev, stream);
 }
@@ -259,6 +275,7 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
                     int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
                     const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
                     kv_stream_t stream) {
+  Range nvtx("kv_gather_layer");
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (layer < 0 || layer >= pool->desc.layer_num || n_seqs < 0 || max_pages < 0 || out_rows < 0)
@@ -280,6 +297,7 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
 
 int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* dst_ids_dev, int64_t n,
             kv_stream_t stream) {
+  Range nvtx("kv_move");
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (n < 0) return KV_ERR_INVALID;
@@ -293,6 +311,7 @@ int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* ds
 int kv_translate_block_table(const kv_pool_t* pool, const int32_t* virt_bt_dev, int32_t n_seqs, int32_t max_pages,
                              const int32_t* seq_len_dev, const int32_t* v2p_dev, int64_t v2p_len,
                              int32_t* out_bt_dev, kv_stream_t stream) {
+  Range nvtx("kv_translate_block_table");
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (n_seqs < 0 || max_pages < 0 || v2p_len < 0) return KV_ERR_INVALID;
@@ -307,6 +326,7 @@ int kv_translate_block_table(const kv_pool_t* pool, const int32_t* virt_bt_dev, 
 }
 
 int kv_pool_last_error(const kv_pool_t* pool, kv_stream_t stream, int32_t* dev_code) {
+  Range nvtx("kv_pool_last_error");
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (dev_code == nullptr) return KV_ERR_INVALID;

@@ -152,6 +152,11 @@ def test_c_abi_round_trip_on_gpu(tmp_path):
     """translate -> store -> gather through the C ABI from a C program."""
     import subprocess
 
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
     exe = c_abi_program(tmp_path, with_cuda=True)
     r = subprocess.run([exe, "gpu"], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
