@@ -5,10 +5,11 @@ workload (L=32 layers, 8 KV heads, head_dim 128, bf16, page size 16, 4096
 pages = an 8 GiB pool):
   1. kv_translate          512 slots -> ids (256 decode tokens + 256 chunk tokens)
   2. kv_store_all_layers   the 256-token chunk into all 32 layers (one launch)
-  3. for each of the 32 layers:
+  3. kv_gather_plan        order the block table's entries by page (once per step)
+  4. for each of the 32 layers:
        kv_store_layer      the 256 decode tokens (one per sequence)
-       kv_gather_layer     256 sequences x 4096 context tokens through block tables
-  4. kv_move               8192 tokens (all 64 row-blocks each) to new slots
+       kv_gather_layer_planned  256 sequences x 4096 context tokens through the block tables
+  5. kv_move               8192 tokens (all 64 row-blocks each) to new slots
 Metric: useful GB/s = algorithmic bytes moved per step (every payload row read
 once and written once, plus index bytes) / step time, with inputs resident in
 HBM. The working set (8 GiB pool, 4 GiB of gather output per layer) is far
@@ -42,8 +43,8 @@ CTX = 4096              # context tokens per sequence
 N_CHUNK = 256           # tokens of a prefill chunk stored into all layers at once
 N_MOVE = 8192           # tokens moved per step
 WORKLOAD = ("llama3-8b-decode: L=32 H_kv=8 D=128 bf16 ps=16 P=4096 (8 GiB pool); step = translate 512 slots, "
-            "store_all_layers 256 chunk tokens, 32 x (store_layer 256 decode tokens + gather 256 seqs x 4096 "
-            "tokens), move 8192 tokens x 64 row-blocks")
+            "store_all_layers 256 chunk tokens, gather plan (page-major order of the block table), 32 x "
+            "(store_layer 256 decode tokens + gather 256 seqs x 4096 tokens), move 8192 tokens x 64 row-blocks")
 
 
 def useful_bytes(shape=SHAPE, n_decode=N_DECODE, ctx=CTX, n_chunk=N_CHUNK, n_move=N_MOVE, n_seqs=None):
@@ -335,24 +336,26 @@ def run_gpu(args):
     mv_src, mv_dst = mv[:N_MOVE], mv[N_MOVE:]
     out_k = torch.empty((g.total, R), dtype=torch.uint8, device=dev)
     out_v = torch.empty_like(out_k)
+    plan = torch.empty(gt.kv_gather_plan_bytes(pool, *g.block_table.shape) // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     gather_ev = []
 
     def step(x, record=False):
         gt.kv_translate(pool, x["slots"], ids, stream=stream)
         gt.kv_store_all_layers(pool, ids[N_DECODE:], x["k_chunk"], x["v_chunk"], stream=stream)
+        gt.kv_gather_plan(pool, x["bt"], x["ln"], plan=plan, stream=stream)
         for layer in range(L):
             gt.kv_store_layer(pool, layer, ids[:N_DECODE], x["k_dec"][layer], x["v_dec"][layer], stream=stream)
             if record:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-            gt.kv_gather_layer(pool, layer, x["bt"], x["ln"], x["cu"], out_k, out_v, stream=stream)
+            gt.kv_gather_layer_planned(pool, layer, plan, x["bt"], x["ln"], x["cu"], out_k, out_v, stream=stream)
             if record:
                 e1.record(stream)
                 gather_ev.append((e0, e1))
         gt.kv_move(pool, mv_src, mv_dst, stream=stream)
-    launches_per_step = 1 + 1 + 2 * L + 1
+    launches_per_step = 1 + 1 + 3 + 2 * L + 1  # the plan is 3 kernels (+ a memset)
 
     for _ in range(args.warmup):
         step(dev_in)
@@ -440,7 +443,7 @@ def run_gpu(args):
                    "useful_bytes_by_kernel": ub, "l2": "no flush: inputs larger than L2 (8 GiB pool, "
                    "4 GiB gather output per layer)", "parallelism": f"replicas x{world}",
                    "pct_of_hbm_peak": round(100 * step_bytes / (ms * 1e-3) / GB / peak, 1)},
-        "roofline": {"bound": "hbm", "kernel": "kv_gather_layer", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "kv_gather_layer_planned", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": gather_bytes, "avg_launch_ms": round(gather_ms, 4)},
@@ -494,11 +497,12 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ per-kernel table
 
-MICRO_DEFAULT = ["translate:2", "block_table:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2", "move:2",
-                 "translate:3", "store:3", "store_slots:3", "store_all:3", "gather:3",
-                 "store:4", "gather:4", "move:4",
-                 "translate:5", "store:5", "store_slots:5", "gather:5", "move:5",
-                 "store:6", "store_all:6", "gather:6", "move:6"]
+MICRO_DEFAULT = ["translate:2", "block_table:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2",
+                 "gather_planned:2", "move:2",
+                 "translate:3", "store:3", "store_slots:3", "store_all:3", "gather:3", "gather_planned:3",
+                 "store:4", "gather:4", "gather_planned:4", "move:4",
+                 "translate:5", "store:5", "store_slots:5", "gather:5", "gather_planned:5", "move:5",
+                 "store:6", "store_all:6", "gather:6", "gather_planned:6", "move:6"]
 
 
 def _payload_torch(gen, rows: int, R: int, itemsize: int, dev):
@@ -675,7 +679,7 @@ def run_micro(args):
             report("store_all_layers", cfg, f"{na} tokens x {L} layers", ms, useful, 2 * L * na,
                    {"l2_flush": flush})
             del Ka, Va
-        if "gather" in kernels:
+        if "gather" in kernels or "gather_planned" in kernels:
             gb = synth.gather_batch(sh) if not args.seqs else synth.GatherBatch(
                 synth.gather_batch(sh).block_table[: args.seqs], np.zeros(args.seqs, np.int32),
                 synth.gather_batch(sh).seq_len[: args.seqs])
@@ -686,10 +690,22 @@ def run_micro(args):
             useful = rows * 2 * kvr * R + rows * 4 // ps
             flush = useful < 4 * l2
             layers = list(range(L)) if cfg != 5 else [0, L - 1]
-            ms = timed(lambda i: gt.kv_gather_layer(pool, layers[i % len(layers)], bt, ln, cu, ok, ov, st),
-                       max(calls, len(layers)), flush)
+            distinct = len(np.unique(gb.block_table))
+            share = {"l2_flush": flush, "distinct_pages": distinct,
+                     "page_reads_per_distinct_page": round(gb.block_table.size / max(1, distinct), 2)}
+            if "gather_planned" in kernels:
+                plan = gt.kv_gather_plan(pool, bt, ln, st)
+                ms = timed(lambda i: gt.kv_gather_layer_planned(pool, layers[i % len(layers)], plan, bt, ln, cu, ok,
+                                                                ov, st), max(calls, len(layers)), flush)
+                msp = timed(lambda i: gt.kv_gather_plan(pool, bt, ln, st, plan=plan), calls, True)
+                report("gather_layer_planned", cfg, f"{gb.block_table.shape[0]} seqs, {rows} rows, page-major plan",
+                       ms, useful, rows, dict(share, plan_build_us=round(statistics.mean(msp) * 1e3, 2)))
+            ms = None
+            if "gather" in kernels:
+                ms = timed(lambda i: gt.kv_gather_layer(pool, layers[i % len(layers)], bt, ln, cu, ok, ov, st),
+                           max(calls, len(layers)), flush)
             ref = None
-            if args.torch_ref:
+            if args.torch_ref and ms is not None:
                 # view rows of every output token, precomputed (not timed)
                 seq = np.repeat(np.arange(gb.block_table.shape[0]), gb.seq_len - gb.seq_start)
                 j = np.concatenate([np.arange(a, b) for a, b in zip(gb.seq_start, gb.seq_len)])
@@ -701,10 +717,9 @@ def run_micro(args):
                     if ov is not None:
                         torch.index_select(view(kvr * layer + 1), 0, vrow, out=ov)
                 ref = timed(ref_gather, max(calls, len(layers)), flush)
-            distinct = len(np.unique(gb.block_table))
-            report("gather_layer", cfg, f"{gb.block_table.shape[0]} seqs, {rows} rows", ms, useful, rows,
-                   {"l2_flush": flush, "distinct_pages": distinct,
-                    "page_reads_per_distinct_page": round(gb.block_table.size / max(1, distinct), 2)}, ref)
+            if ms is not None:
+                report("gather_layer", cfg, f"{gb.block_table.shape[0]} seqs, {rows} rows", ms, useful, rows, share,
+                       ref)
             del ok, ov
         if "move" in kernels:
             src, dst = synth.move_slots(sh)

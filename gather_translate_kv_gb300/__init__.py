@@ -113,6 +113,9 @@ def lib():
         "kv_store_all_layers_slots": [vp, vp, i64, vp, i64, vp, vp, vp],
         "kv_gather_layer": [vp, i32, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
         "kv_move": [vp, vp, vp, i64, vp],
+        "kv_gather_plan_bytes": [vp, i32, i32, P(i64)],
+        "kv_gather_plan": [vp, vp, i32, i32, vp, vp, vp, i64, vp],
+        "kv_gather_layer_planned": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
         "kv_translate_block_table": [vp, vp, i32, i32, vp, vp, i64, vp, vp],
         "kv_pool_last_error": [vp, vp, P(i32)],
     }
@@ -290,6 +293,42 @@ def kv_gather_layer(pool: KVPool, layer: int, block_table: torch.Tensor, seq_len
         _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
         _dev(cu_out, "cu_out", torch.int64), _dev(out_k, "out_k"), _dev(out_v, "out_v"), ob // R,
         _stream(stream)))
+
+
+def kv_gather_plan_bytes(pool: KVPool, n_seqs: int, max_pages: int) -> int:
+    out = ctypes.c_int64()
+    _check("kv_gather_plan_bytes", lib().kv_gather_plan_bytes(pool.handle, n_seqs, max_pages, ctypes.byref(out)))
+    return out.value
+
+
+def kv_gather_plan(pool: KVPool, block_table: torch.Tensor, seq_len: torch.Tensor,
+                   seq_start: torch.Tensor | None = None, plan: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """Page-major plan of a block table (an int32 device tensor, allocated
+    here when not given); reuse it for every layer's gather of the step."""
+    n_seqs, max_pages = block_table.shape
+    nbytes = kv_gather_plan_bytes(pool, n_seqs, max_pages)
+    if plan is None:
+        plan = torch.empty(nbytes // 4, dtype=torch.int32, device=block_table.device)
+    _check("kv_gather_plan", lib().kv_gather_plan(
+        pool.handle, _dev(block_table, "block_table", torch.int32), n_seqs, max_pages,
+        _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
+        _dev(plan, "plan", torch.int32), plan.numel() * 4, _stream(stream)))
+    return plan
+
+
+def kv_gather_layer_planned(pool: KVPool, layer: int, plan: torch.Tensor, block_table: torch.Tensor,
+                            seq_len: torch.Tensor, cu_out: torch.Tensor, out_k: torch.Tensor,
+                            out_v: torch.Tensor | None, seq_start: torch.Tensor | None = None, stream=None) -> None:
+    n_seqs, max_pages = block_table.shape
+    R = pool.row_bytes
+    ob = out_k.numel() * out_k.element_size()
+    if ob % R != 0 or (out_v is not None and out_v.numel() * out_v.element_size() != ob):
+        raise ValueError("out_k and out_v must be the same size, a whole number of rows")
+    _check("kv_gather_layer_planned", lib().kv_gather_layer_planned(
+        pool.handle, layer, _dev(plan, "plan", torch.int32), _dev(block_table, "block_table", torch.int32),
+        n_seqs, max_pages, _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
+        _dev(cu_out, "cu_out", torch.int64), _dev(out_k, "out_k"), _dev(out_v, "out_v"), ob // R, _stream(stream)))
 
 
 def kv_move(pool: KVPool, src_ids: torch.Tensor, dst_ids: torch.Tensor, stream=None) -> None:

@@ -271,15 +271,14 @@ int kv_store_all_layers_slots(const kv_pool_t* pool, const int64_t* slots_dev, i
   return store_slots(pool, 0, pool->desc.layer_num, slots_dev, n, v2p_dev, v2p_len, k_all_dev, v_all_dev, stream);
 }
 
-int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_table_dev, int32_t n_seqs,
-                    int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
-                    const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
-                    kv_stream_t stream) {
-  Range nvtx("kv_gather_layer");
+static int gather(const kv_pool_t* pool, int32_t layer, const void* plan_dev, const int32_t* block_table_dev,
+                  int32_t n_seqs, int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
+                  const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream) {
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (layer < 0 || layer >= pool->desc.layer_num || n_seqs < 0 || max_pages < 0 || out_rows < 0)
     return KV_ERR_INVALID;
+  if (static_cast<int64_t>(n_seqs) * max_pages >= (int64_t(1) << 31)) return KV_ERR_INVALID;
   if (n_seqs == 0) return KV_OK;
   if (seq_len_dev == nullptr || cu_out_dev == nullptr || (block_table_dev == nullptr && max_pages > 0))
     return KV_ERR_INVALID;
@@ -288,11 +287,57 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
     return KV_ERR_INVALID;
   if ((out_k_dev && !aligned16(out_k_dev)) || (out_v_dev && !aligned16(out_v_dev)) ||
       (reinterpret_cast<uintptr_t>(cu_out_dev) & 7u) || (reinterpret_cast<uintptr_t>(seq_len_dev) & 3u) ||
-      (reinterpret_cast<uintptr_t>(block_table_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_start_dev) & 3u))
+      (reinterpret_cast<uintptr_t>(block_table_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_start_dev) & 3u) ||
+      (reinterpret_cast<uintptr_t>(plan_dev) & 3u))
     return KV_ERR_ALIGN;
   return launched(gtkv::launch_gather(pool->dev, layer, block_table_dev, n_seqs, max_pages, seq_start_dev,
-                                      seq_len_dev, cu_out_dev, out_k_dev, out_v_dev, out_rows, pool->sm_count,
-                                      as_stream(stream)));
+                                      seq_len_dev, cu_out_dev, out_k_dev, out_v_dev, out_rows,
+                                      static_cast<const int32_t*>(plan_dev), pool->sm_count, as_stream(stream)));
+}
+
+int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_table_dev, int32_t n_seqs,
+                    int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
+                    const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
+                    kv_stream_t stream) {
+  Range nvtx("kv_gather_layer");
+  return gather(pool, layer, nullptr, block_table_dev, n_seqs, max_pages, seq_start_dev, seq_len_dev, cu_out_dev,
+                out_k_dev, out_v_dev, out_rows, stream);
+}
+
+int kv_gather_plan_bytes(const kv_pool_t* pool, int32_t n_seqs, int32_t max_pages, int64_t* plan_bytes) {
+  if (pool == nullptr || plan_bytes == nullptr || n_seqs < 0 || max_pages < 0) return KV_ERR_INVALID;
+  if (static_cast<int64_t>(n_seqs) * max_pages >= (int64_t(1) << 31)) return KV_ERR_INVALID;
+  *plan_bytes = 4 * gtkv::plan_words(pool->dev, n_seqs, max_pages);
+  return KV_OK;
+}
+
+int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
+                   const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,
+                   kv_stream_t stream) {
+  Range nvtx("kv_gather_plan");
+  int rc = enter(pool);
+  if (rc != KV_OK) return rc;
+  int64_t need = 0;
+  if ((rc = kv_gather_plan_bytes(pool, n_seqs, max_pages, &need)) != KV_OK) return rc;
+  if (plan_dev == nullptr || plan_bytes < need) return KV_ERR_INVALID;
+  if (n_seqs > 0 && (seq_len_dev == nullptr || (block_table_dev == nullptr && max_pages > 0)))
+    return KV_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(plan_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_len_dev) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_start_dev) & 3u))
+    return KV_ERR_ALIGN;
+  return launched(gtkv::launch_gather_plan(pool->dev, block_table_dev, n_seqs, max_pages, seq_start_dev,
+                                           seq_len_dev, static_cast<int32_t*>(plan_dev), pool->sm_count,
+                                           as_stream(stream)));
+}
+
+int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* plan_dev,
+                            const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
+                            const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
+                            void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream) {
+  Range nvtx("kv_gather_layer_planned");
+  if (plan_dev == nullptr) return KV_ERR_INVALID;
+  return gather(pool, layer, plan_dev, block_table_dev, n_seqs, max_pages, seq_start_dev, seq_len_dev, cu_out_dev,
+                out_k_dev, out_v_dev, out_rows, stream);
 }
 
 int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* dst_ids_dev, int64_t n,

@@ -46,8 +46,8 @@ __device__ __forceinline__ void check_gather_meta(const DevPool& p, int32_t n_se
   if (tid == 0 && __ldg(cu + n_seqs) > out_rows) atomicOr(p.err, KV_DEV_ERR_TABLE);
 }
 
-// One work item: chunk c of block-table entry (s, k), clipped to the window
-// [start_s, len_s), to tokens >= 0 and to output rows [0, out_rows).
+// One work item: chunk c of block-table entry sk = s*max_pages + k, clipped to
+// the window [start_s, len_s), to tokens >= 0 and to output rows [0, out_rows).
 struct Run {
   int64_t src;   // 16-byte vector index (from p.base) of its first K row; V is ps rows later
   int64_t row;   // first output row
@@ -55,15 +55,13 @@ struct Run {
   int kind;      // 0: nothing to copy; 1: rows of a page; 2: tombstoned entry, every row reads the sink
 };
 
-__device__ __forceinline__ Run gather_item(const DevPool& p, int64_t it, int64_t koff, const int32_t* __restrict__ bt,
-                                           int32_t max_pages, const int32_t* __restrict__ seq_start,
+__device__ __forceinline__ Run gather_item(const DevPool& p, int64_t sk, int64_t c, int64_t koff,
+                                           const int32_t* __restrict__ bt, int32_t max_pages,
+                                           const int32_t* __restrict__ seq_start,
                                            const int32_t* __restrict__ seq_len, const int64_t* __restrict__ cu,
-                                           int64_t out_rows, int32_t chunk_rows, int32_t chunks_per_page,
-                                           bool report) {
+                                           int64_t out_rows, int32_t chunk_rows, bool report) {
   Run r{0, 0, 0, 0};
   const int64_t ps = p.ps;
-  const int64_t sk = it / chunks_per_page;  // block-table entry index s*max_pages + k
-  const int64_t c = it - sk * chunks_per_page;
   const int64_t s = sk / max_pages;
   const int64_t k = sk - s * max_pages;
   const int64_t a = seq_start ? __ldg(seq_start + s) : 0;
@@ -102,31 +100,60 @@ __device__ __forceinline__ Run gather_item(const DevPool& p, int64_t it, int64_t
 }
 
 
-// Items = (sequence s, table entry k, chunk c). CHV 16-byte vectors per lane
-// per round: one round moves 32*CHV vectors of K and as many of V.
-template <int CHV>
+// Items = (table entry sk, chunk c), taken in table order, or in the order of
+// a page-major plan (PLANNED: kv_plan.cu). CHV 16-byte vectors per lane per
+// round: one round moves 32*CHV vectors of K and as many of V.
+template <int CHV, bool PLANNED>
 __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer, const int32_t* __restrict__ bt,
                                                         int32_t n_seqs, int32_t max_pages,
                                                         const int32_t* __restrict__ seq_start,
                                                         const int32_t* __restrict__ seq_len,
                                                         const int64_t* __restrict__ cu, uint4* __restrict__ out_k,
                                                         uint4* __restrict__ out_v, int64_t out_rows,
-                                                        int32_t chunk_rows, int32_t chunks_per_page) {
+                                                        int32_t chunk_rows, int32_t chunks_per_page,
+                                                        const int32_t* __restrict__ plan) {
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   check_gather_meta(p, n_seqs, max_pages, seq_start, seq_len, cu, out_rows, tid, nthreads);
+  const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
+  int64_t n_units = n_entries;  // entries (table order) or plan positions
+  const int32_t* order = nullptr;
+  if constexpr (PLANNED) {
+    // the plan must have been built for a table of this shape; its entries
+    // are bounds-checked one by one below, so a stale plan can only give
+    // wrong rows (flagged), never an access outside the buffers
+    if (__ldg(plan + 1) != n_seqs || __ldg(plan + 2) != max_pages) {
+      if (tid == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
+      return;
+    }
+    if (__ldg(plan + 3) != 0) {  // page-major order pays; else keep the table's order
+      const int64_t np = __ldg(plan);
+      n_units = np < 0 ? 0 : (np > n_entries ? n_entries : np);
+      order = plan + 4 + p.num_pages + 1;
+    }
+  }
 
   const int lane = threadIdx.x & 31;
   const int64_t vpr = p.vpr;
   const int64_t ps_vec = p.ps * vpr;                                      // K -> V distance, in vectors
   const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * p.ps;  // K (or latent) block of the layer
   const bool has_v = p.kv_rows == 2;
-  const int64_t n_items = static_cast<int64_t>(n_seqs) * max_pages * chunks_per_page;
+  const int64_t n_items = n_units * chunks_per_page;
   const L2Policy pol = make_l2_policy();
 
   for (int64_t it = tid >> 5; it < n_items; it += nthreads >> 5) {
-    const Run r = gather_item(p, it, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows,
-                              chunks_per_page, lane == 0);
+    const int64_t u = it / chunks_per_page;
+    const int64_t c = it - u * chunks_per_page;
+    int64_t sk = u;
+    if (PLANNED && order != nullptr) {
+      sk = __ldg(order + u);
+      if (sk < 0 || sk >= n_entries) {
+        if (lane == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
+        continue;
+      }
+    }
+    const Run r = gather_item(p, sk, c, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows,
+                              lane == 0);
     if (r.kind == 0) continue;
     uint4* dk = out_k + r.row * vpr;
     uint4* dv = has_v ? out_v + r.row * vpr : nullptr;
@@ -300,8 +327,9 @@ __global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
     uint32_t bytes = 0;
     bool sink = false;
     if (it < n_items) {
-      const Run r = gather_item(p, it, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows,
-                                chunks_per_page, true);
+      const int64_t sk = it / chunks_per_page;
+      const Run r = gather_item(p, sk, it - sk * chunks_per_page, koff, bt, max_pages, seq_start, seq_len, cu,
+                                out_rows, chunk_rows, true);
       if (r.kind != 0) {
         src = r.src;
         row = r.row;
@@ -350,13 +378,13 @@ __global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
 
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
                           const int32_t* seq_start, const int32_t* seq_len, const int64_t* cu, void* out_k,
-                          void* out_v, int64_t out_rows, int sm_count, cudaStream_t s) {
+                          void* out_v, int64_t out_rows, const int32_t* plan, int sm_count, cudaStream_t s) {
   constexpr int CHV = 8;  // one round = 32 lanes x 8 vectors = 4 KiB of K and 4 KiB of V in flight per warp
   int64_t chunk_rows = GTKV_GATHER_CHUNK / (16 * p.vpr);
   if (chunk_rows < 1) chunk_rows = 1;
   if (chunk_rows > p.ps) chunk_rows = p.ps;
   const int64_t cpp = (p.ps + chunk_rows - 1) / chunk_rows;
-  if (GTKV_GATHER_BULK && chunk_rows * 16 * p.vpr <= kBulkHalf) {
+  if (GTKV_GATHER_BULK && plan == nullptr && chunk_rows * 16 * p.vpr <= kBulkHalf) {
     constexpr int threads = 32 * GTKV_BULK_WARPS;
     constexpr size_t smem = static_cast<size_t>(GTKV_BULK_WARPS) * GTKV_BULK_STAGES * (kBulkStage + 8);
     static bool attr = false;
@@ -378,14 +406,14 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
         static_cast<uint4*>(out_v), out_rows, static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp));
     return cudaGetLastError();
   }
-  auto kernel = k_gather_runs<CHV>;
+  auto kernel = plan ? k_gather_runs<CHV, true> : k_gather_runs<CHV, false>;
   int64_t warps = static_cast<int64_t>(n_seqs) * max_pages * cpp;
   const int64_t seq_warps = (static_cast<int64_t>(n_seqs) + 31) / 32;
   if (warps < seq_warps) warps = seq_warps;
   const unsigned grid = grid_for(kernel, warps, sm_count);
   kernel<<<grid, kBlock, 0, s>>>(p, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu,
                                  static_cast<uint4*>(out_k), static_cast<uint4*>(out_v), out_rows,
-                                 static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp));
+                                 static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp), plan);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,151 @@
+// Page-major gather plan: the block-table entries of a batch, ordered by the
+// page they name.
+//
+// Many sequences often share pages (common prefixes; in the decode workload
+// every page is named by ~16 sequences). A gather that walks the table
+// sequence by sequence reads a shared page at ~16 unrelated moments, so L2
+// rarely still holds it. Walking the entries page by page instead brings all
+// readers of a page together in time: L2 merges their reads and DRAM delivers
+// each page about once. The order depends only on the block table, which all
+// layers share, so one plan serves every layer's gather of a step.
+//
+// The plan is a counting sort of the entries by page, in a caller-provided
+// buffer (int32 words):
+//   [0] number of entries in the plan   [1] n_seqs   [2] max_pages
+//   [3] 1 when the page-major order pays (entries >= 1.5 x distinct pages),
+//       0 when pages are hardly shared and the table's own order is better
+//       (the output writes stay sequential); the planned gather follows it
+//   [4 .. 4+P]            per-page counts, then start offsets (P + 1 words)
+//   [5+P .. 5+P+S*maxp)   entry indices s*max_pages + k, grouped by page
+// Only entries whose tokens overlap the sequence's window [start, len) enter
+// the plan. A tombstoned entry (negative page) reads the sink on page 0 and
+// is grouped with page 0; a page >= P raises KV_DEV_ERR_ROW and is left out.
+#include "kv_launch.h"
+
+namespace gtkv {
+
+namespace {
+
+constexpr int kPlanHeader = 4;
+
+// Page bucket of entry e, or -1 when it holds no token of the window.
+__device__ __forceinline__ int64_t plan_bucket(const DevPool& p, int64_t e, const int32_t* __restrict__ bt,
+                                               int32_t max_pages, const int32_t* __restrict__ seq_start,
+                                               const int32_t* __restrict__ seq_len, int& bits) {
+  const int64_t s = e / max_pages;
+  const int64_t k = e - s * max_pages;
+  int64_t a = seq_start ? __ldg(seq_start + s) : 0;
+  if (a < 0) a = 0;
+  const int64_t b = __ldg(seq_len + s);
+  if (k * p.ps >= b || (k + 1) * p.ps <= a) return -1;
+  const int64_t page = __ldg(bt + e);
+  if (page >= p.num_pages) {
+    bits |= KV_DEV_ERR_ROW;
+    return -1;
+  }
+  return page < 0 ? 0 : page;
+}
+
+__global__ void __launch_bounds__(kBlock) k_plan_count(DevPool p, const int32_t* __restrict__ bt, int64_t n_entries,
+                                                       int32_t max_pages, const int32_t* __restrict__ seq_start,
+                                                       const int32_t* __restrict__ seq_len, int32_t* __restrict__ plan) {
+  int32_t* counts = plan + kPlanHeader;
+  int bits = 0;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
+    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
+    if (b >= 0) atomicAdd(counts + b, 1);
+  }
+  if (bits) atomicOr(p.err, bits);
+}
+
+// Exclusive scan of the P counts into start offsets, one block of 1024
+// threads, each owning a contiguous segment; the total goes to the header.
+__global__ void __launch_bounds__(1024) k_plan_scan(int64_t n_buckets, int32_t n_seqs, int32_t max_pages,
+                                                    int32_t* __restrict__ plan) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t used_pages;
+  int32_t* counts = plan + kPlanHeader;
+  const int t = threadIdx.x;
+  if (t == 0) used_pages = 0;
+  const int64_t seg = (n_buckets + blockDim.x - 1) / blockDim.x;
+  const int64_t lo = t * seg < n_buckets ? t * seg : n_buckets;
+  const int64_t hi = lo + seg < n_buckets ? lo + seg : n_buckets;
+  int32_t sum = 0, used = 0;
+  for (int64_t i = lo; i < hi; ++i) {
+    sum += counts[i];
+    used += counts[i] > 0;
+  }
+  __syncthreads();
+  if (used) atomicAdd(&used_pages, used);
+  // block-wide exclusive scan of the per-thread sums
+  const int lane = t & 31, w = t >> 5;
+  int32_t incl = sum;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t v = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int32_t ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t v = __shfl_up_sync(kFull, ws, d);
+      if (lane >= d) ws += v;
+    }
+    warp_sums[lane] = ws;  // inclusive over warps
+  }
+  __syncthreads();
+  int32_t run = incl - sum + (w > 0 ? warp_sums[w - 1] : 0);  // exclusive prefix of this segment
+  for (int64_t i = lo; i < hi; ++i) {
+    const int32_t c = counts[i];
+    counts[i] = run;
+    run += c;
+  }
+  if (t == static_cast<int>(blockDim.x) - 1) {
+    counts[n_buckets] = run;  // == total
+    plan[0] = run;
+    plan[1] = n_seqs;
+    plan[2] = max_pages;
+    plan[3] = 2 * static_cast<int64_t>(run) >= 3 * static_cast<int64_t>(used_pages) ? 1 : 0;
+  }
+}
+
+__global__ void __launch_bounds__(kBlock) k_plan_scatter(DevPool p, const int32_t* __restrict__ bt,
+                                                         int64_t n_entries, int32_t max_pages,
+                                                         const int32_t* __restrict__ seq_start,
+                                                         const int32_t* __restrict__ seq_len,
+                                                         int32_t* __restrict__ plan) {
+  int32_t* offs = plan + kPlanHeader;
+  int32_t* entries = offs + p.num_pages + 1;
+  int bits = 0;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
+    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
+    if (b >= 0) entries[atomicAdd(offs + b, 1)] = static_cast<int32_t>(e);
+  }
+  // page >= P entries were already reported by the count pass
+}
+
+}  // namespace
+
+int64_t plan_words(const DevPool& p, int32_t n_seqs, int32_t max_pages) {
+  return kPlanHeader + p.num_pages + 1 + static_cast<int64_t>(n_seqs) * max_pages;
+}
+
+cudaError_t launch_gather_plan(const DevPool& p, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
+                               const int32_t* seq_start, const int32_t* seq_len, int32_t* plan, int sm_count,
+                               cudaStream_t s) {
+  const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
+  cudaError_t e = cudaMemsetAsync(plan, 0, sizeof(int32_t) * (kPlanHeader + p.num_pages + 1), s);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = grid_for(k_plan_count, (n_entries + 31) / 32, sm_count);
+  k_plan_count<<<grid, kBlock, 0, s>>>(p, bt, n_entries, max_pages, seq_start, seq_len, plan);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_plan_scan<<<1, 1024, 0, s>>>(p.num_pages, n_seqs, max_pages, plan);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_plan_scatter<<<grid, kBlock, 0, s>>>(p, bt, n_entries, max_pages, seq_start, seq_len, plan);
+  return cudaGetLastError();
+}
+
+}  // namespace gtkv

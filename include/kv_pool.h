@@ -260,6 +260,42 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
                     const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
                     kv_stream_t stream);
 
+/* Page-major gather plan. Many sequences often share pages (common
+ * prefixes); a gather that visits the block table sequence by sequence reads
+ * a shared page at unrelated times. kv_gather_plan orders the entries of a
+ * block table by the page they name (a counting sort), and
+ * kv_gather_layer_planned then visits them in that order, so all readers of a
+ * page run together and L2 serves the repeats. The plan depends only on the
+ * table and the windows, so one plan serves every layer of a step.
+ * Source: the read path of the report (功能与动机: one contiguous tensor and
+ * one shared block table per layer); the ordering is this library's.
+ *
+ * kv_gather_plan_bytes: size of the plan buffer for a table of n_seqs x
+ *   max_pages entries: 4 * (4 + num_pages + 1 + n_seqs * max_pages) bytes
+ *   (host only). n_seqs * max_pages must be < 2^31.
+ * kv_gather_plan: builds the plan into plan_dev (device, plan_bytes long,
+ *   4-byte aligned; the caller owns it and may reuse it until the table
+ *   changes). Layout (int32): [0] entries in the plan, [1] n_seqs,
+ *   [2] max_pages, [3] 1 when the page-major order pays (entries >= 1.5 x
+ *   distinct pages) else 0, then num_pages + 1 per-page offsets (the sort's
+ *   workspace), then the entry indices s * max_pages + k grouped by page.
+ *   With [3] = 0 (pages hardly shared) the planned gather keeps the table's
+ *   own order, whose output writes stay sequential.
+ *   Only entries holding tokens of [start_s, len_s) enter the plan; an entry
+ *   naming a page >= num_pages sets KV_DEV_ERR_ROW and is left out.
+ * kv_gather_layer_planned: kv_gather_layer with the same arguments plus the
+ *   plan built from the same block table, starts and lengths; the output is
+ *   identical. A plan built for another table shape sets KV_DEV_ERR_TABLE and
+ *   writes nothing; plan entries are bounds-checked one by one. */
+int kv_gather_plan_bytes(const kv_pool_t* pool, int32_t n_seqs, int32_t max_pages, int64_t* plan_bytes);
+int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
+                   const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,
+                   kv_stream_t stream);
+int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* plan_dev,
+                            const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
+                            const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
+                            void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream);
+
 /* Move: copy every row-block (all layers' K and V, 2L rows) of token
  * src_ids[i] to token dst_ids[i].
  * Source: move_kv_cache / _move_kv_cache_impl (关键文件 memory_pool.py).

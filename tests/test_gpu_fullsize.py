@@ -128,13 +128,20 @@ class Full:
             exp[hit] = srows[order[pos[hit]]]
         return exp
 
-    def check_gather(self, layer, gb: synth.GatherBatch, stored: list):
+    def check_gather(self, layer, gb: synth.GatherBatch, stored: list, planned: bool = False):
+        """Gather one layer (table order, or through a page-major plan) and
+        compare every output row with the oracle's source offsets."""
         ks, vs, err = self.o.gather_rows(layer, gb.block_table, gb.seq_len, gb.cu, gb.seq_start)
         assert err == 0 and (ks >= 0).all()
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
         ok = torch.empty((gb.total, self.R), dtype=torch.uint8, device="cuda")
         ov = torch.empty_like(ok)
-        gt.kv_gather_layer(self.pool, layer, d(gb.block_table), d(gb.seq_len), d(gb.cu), ok, ov, d(gb.seq_start))
+        bt, ln, cu, st = d(gb.block_table), d(gb.seq_len), d(gb.cu), d(gb.seq_start)
+        if planned:
+            plan = gt.kv_gather_plan(self.pool, bt, ln, st)
+            gt.kv_gather_layer_planned(self.pool, layer, plan, bt, ln, cu, ok, ov, st)
+        else:
+            gt.kv_gather_layer(self.pool, layer, bt, ln, cu, ok, ov, st)
         assert gt.kv_pool_last_error(self.pool) == 0
         assert torch.equal(ok, self.expected_reads(ks, stored[0])), f"gathered K of layer {layer} differs"
         assert torch.equal(ov, self.expected_reads(vs, stored[1])), f"gathered V of layer {layer} differs"
@@ -161,6 +168,7 @@ def test_decode_llama3_8b_full():
         stored[layer] = ((kd, Kd), (vd, Vd))
     for layer in (0, 17, 31):
         F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]))
+        F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]), planned=True)
     # move 8192 never-stored tokens to other never-stored tokens
     used = np.unique(np.concatenate([synth.store_slots(sh, l) for l in range(sh.layer_num)]))
     src, dst = synth.move_slots(sh, 8192, avoid=used)
@@ -219,7 +227,7 @@ def test_swa_fp8_full():
     for layer in range(sh.layer_num):
         K, V = _vals(sh, slots.size, layer)
         kd, vd, Kd, Vd = F.check_store(layer, slots, K, V, ids)
-        F.check_gather(layer, gb, ([(kd, Kd)], [(vd, Vd)]))
+        F.check_gather(layer, gb, ([(kd, Kd)], [(vd, Vd)]), planned=layer % 2 == 1)
     used = np.unique(gb.block_table.astype(np.int64)[:, :, None] * sh.page_size + np.arange(sh.page_size))
     src, dst = synth.move_slots(sh, 8192, avoid=used)
     src = np.setdiff1d(src, used)[:8000]
@@ -259,6 +267,6 @@ def test_id_bound_stress_full():
     gb = synth.gather_batch(sh)
     assert (gb.block_table == sh.num_pages - 1).any()
     for layer in (0, 79):
-        F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]))
+        F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]), planned=layer == 79)
     F.check_untouched()
     F.close()

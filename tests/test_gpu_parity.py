@@ -531,3 +531,64 @@ def test_library_owned_buffer_round_trip():
     assert np.array_equal(dk.cpu().numpy(), as_rows(K, shape.row_bytes))
     assert np.array_equal(dv.cpu().numpy(), as_rows(V, shape.row_bytes))
     gt.kv_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("shape,anchor,latent", [(s, a, False) for s, a in SHAPES[:8]] + [(MLA_SHAPES[0][0], 0, True)],
+                         ids=IDS[:8] + [MLA_SHAPES[0][0].name])
+def test_planned_gather_matches_oracle(shape, anchor, latent):
+    """kv_gather_plan + kv_gather_layer_planned: the plan holds every entry
+    that has tokens in its sequence's window exactly once, grouped by page,
+    and the planned gather writes exactly what the oracle's gather writes."""
+    rng = np.random.default_rng(600 + shape.row_bytes + shape.page_size)
+    pp = PoolPair(shape, anchor, latent=latent)
+    o, R, L, ps, P = pp.o, pp.R, shape.layer_num, shape.page_size, shape.num_pages
+    S_, maxp = 23, min(P - 1, 6)
+    # heavily shared pages: every sequence draws from a few pages
+    bt = rng.integers(1, min(P, 5), size=(S_, maxp)).astype(np.int32)
+    bt[3, 1] = -1  # a tombstoned entry reads the sink
+    ln = rng.integers(0, maxp * ps + 1, size=S_).astype(np.int32)
+    ln[0], ln[5] = maxp * ps, 0
+    st = np.minimum(rng.integers(0, 2 * ps, size=S_), ln).astype(np.int32)
+    g = synth.GatherBatch(bt, st, ln)
+    plan = gt.kv_gather_plan(pp.pool, to_dev(bt), to_dev(ln), to_dev(st))
+    assert pp.last_error() == 0
+    h = plan.cpu().numpy()
+    n_valid, entries = int(h[0]), h[4 + P + 1:]
+    want = [s * maxp + k for s in range(S_) for k in range(maxp) if k * ps < ln[s] and (k + 1) * ps > st[s]]
+    assert (h[1], h[2]) == (S_, maxp) and n_valid == len(want)
+    assert h[3] == 1, "pages this shared should be walked page by page"
+    assert sorted(entries[:n_valid].tolist()) == sorted(want)
+    pages = np.maximum(bt.reshape(-1)[entries[:n_valid]], 0)
+    assert np.all(np.diff(pages) >= 0), "plan entries are not grouped by page"
+    for layer in sorted({0, L - 1}):
+        rows = g.total + 2
+        ok = np.full((rows, R), 0x11, np.uint8)
+        ov = None if latent else np.full((rows, R), 0x22, np.uint8)
+        ok, ov, err = o.gather(pp.M, layer, bt, ln, g.cu, st, rows, ok, ov)
+        dk = torch.full((rows, R), 0x11, dtype=torch.uint8, device="cuda")
+        dv = None if latent else torch.full((rows, R), 0x22, dtype=torch.uint8, device="cuda")
+        gt.kv_gather_layer_planned(pp.pool, layer, plan, to_dev(bt), to_dev(ln), to_dev(g.cu), dk, dv, to_dev(st))
+        assert err == 0 and pp.last_error() == 0
+        assert_bytes_equal(dk.cpu().numpy(), ok, f"planned gather K layer {layer}", R)
+        if not latent:
+            assert_bytes_equal(dv.cpu().numpy(), ov, f"planned gather V layer {layer}", R)
+    # distinct pages: the plan says to keep the table's order, and the planned
+    # gather still matches the oracle
+    if P - 1 >= S_ * maxp:
+        btd = (1 + rng.permutation(P - 1)[: S_ * maxp]).reshape(S_, maxp).astype(np.int32)
+        pd = gt.kv_gather_plan(pp.pool, to_dev(btd), to_dev(ln), to_dev(st))
+        assert int(pd.cpu()[3]) == 0
+        ok, ov, err = o.gather(pp.M, 0, btd, ln, g.cu, st, g.total)
+        dk = torch.zeros((g.total, R), dtype=torch.uint8, device="cuda")
+        dv = None if latent else torch.zeros((g.total, R), dtype=torch.uint8, device="cuda")
+        gt.kv_gather_layer_planned(pp.pool, 0, pd, to_dev(btd), to_dev(ln), to_dev(g.cu), dk, dv, to_dev(st))
+        assert err == 0 and pp.last_error() == 0
+        assert_bytes_equal(dk.cpu().numpy(), ok, "planned gather, table order", R)
+    # a plan built for another table shape is refused on the device, nothing written
+    other = gt.kv_gather_plan(pp.pool, to_dev(bt[:, :-1]), to_dev(np.minimum(ln, (maxp - 1) * ps)))
+    dk = torch.full((g.total, R), 0x33, dtype=torch.uint8, device="cuda")
+    dv = None if latent else torch.full((g.total, R), 0x33, dtype=torch.uint8, device="cuda")
+    gt.kv_gather_layer_planned(pp.pool, 0, other, to_dev(bt), to_dev(ln), to_dev(g.cu), dk, dv, to_dev(st))
+    assert pp.last_error() == gt.KV_DEV_ERR_TABLE
+    assert bool((dk == 0x33).all())
+    pp.close()
