@@ -27,6 +27,7 @@ KV_OK = 0
 STATUS = {
     0: "KV_OK", -1: "KV_ERR_INVALID", -2: "KV_ERR_ASYMMETRIC", -3: "KV_ERR_ID_BOUND",
     -4: "KV_ERR_TAIL_PAD", -5: "KV_ERR_ALIGN", -6: "KV_ERR_CUDA", -7: "KV_ERR_DEVICE",
+    -8: "KV_ERR_CAPACITY",
 }
 KV_DEV_ERR_ROW, KV_DEV_ERR_V2P, KV_DEV_ERR_TABLE, KV_DEV_ERR_FORM = 1, 2, 4, 8
 
@@ -115,6 +116,7 @@ def lib():
         "kv_move": [vp, vp, vp, i64, vp],
         "kv_gather_plan_bytes": [vp, i32, i32, P(i64)],
         "kv_gather_plan": [vp, vp, i32, i32, vp, vp, vp, i64, vp],
+        "kv_gather_plan_noalloc": [vp, vp, i32, i32, vp, vp, vp, i64, vp],
         "kv_gather_layer_planned": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
         "kv_translate_block_table": [vp, vp, i32, i32, vp, vp, i64, vp, vp],
         "kv_pool_last_error": [vp, vp, P(i32)],
@@ -311,6 +313,22 @@ def kv_gather_plan(pool: KVPool, block_table: torch.Tensor, seq_len: torch.Tenso
     if plan is None:
         plan = torch.empty(nbytes // 4, dtype=torch.int32, device=block_table.device)
     _check("kv_gather_plan", lib().kv_gather_plan(
+        pool.handle, _dev(block_table, "block_table", torch.int32), n_seqs, max_pages,
+        _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
+        _dev(plan, "plan", torch.int32), plan.numel() * 4, _stream(stream)))
+    return plan
+
+
+def kv_gather_plan_noalloc(pool: KVPool, block_table: torch.Tensor, seq_len: torch.Tensor, plan: torch.Tensor,
+                           seq_start: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kv_gather_plan for callers that cannot allocate device memory: the plan
+    buffer (int32, at least kv_gather_plan_bytes() long) is theirs, and the
+    sort's counters live in a fixed array of the library (pools of at most
+    65536 pages, else KV_ERR_CAPACITY). Nothing is allocated here either.
+    Calls that overlap on the GPU share that array and race; the first call
+    on a device looks up its address and should precede any stream capture."""
+    n_seqs, max_pages = block_table.shape
+    _check("kv_gather_plan_noalloc", lib().kv_gather_plan_noalloc(
         pool.handle, _dev(block_table, "block_table", torch.int32), n_seqs, max_pages,
         _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
         _dev(plan, "plan", torch.int32), plan.numel() * 4, _stream(stream)))

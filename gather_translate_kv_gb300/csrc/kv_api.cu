@@ -10,18 +10,7 @@
 #include "kv_launch.h"
 #include "kv_layout.h"
 #include "kv_pool.h"
-
-struct kv_pool {
-  kv_pool_desc desc;
-  gtkv::Layout lay;
-  uint8_t* raw;
-  int64_t raw_bytes;
-  int owns_raw;
-  int32_t* d_err;
-  int device;
-  int sm_count;
-  gtkv::DevPool dev;
-};
+#include "kv_pool_internal.h"
 
 namespace {
 
@@ -69,6 +58,7 @@ const char* kv_status_string(int status) {
     case KV_ERR_ALIGN: return "KV_ERR_ALIGN";
     case KV_ERR_CUDA: return "KV_ERR_CUDA";
     case KV_ERR_DEVICE: return "KV_ERR_DEVICE";
+    case KV_ERR_CAPACITY: return "KV_ERR_CAPACITY";
     default: return "KV_ERR_UNKNOWN";
   }
 }

@@ -1,0 +1,200 @@
+// kv_gather_plan_noalloc: the page-major gather plan of kv_plan.cu, built
+// without device memory from the caller beyond the plan itself.
+//
+// Some callers of this library cannot call cudaMalloc: code inside a host
+// framework whose allocator reserved the device's memory at start-up and owns
+// it, or a serving loop that must keep allocations (and the device-wide
+// synchronization cudaMalloc and cudaFree may cause) out of its steady state.
+// kv_gather_plan counts the entries of each page inside the caller's plan
+// buffer; this variant counts in g_plan_counts, a fixed array in the
+// library's device image, and copies the finished per-page offsets into the
+// plan, so the plan matches kv_gather_plan's up to the order of the entries
+// within one page.
+//
+// g_plan_counts holds kMaxPages + 1 int32 counters (256 KiB + 4 bytes); every
+// GPU that loads the library keeps it until the process exits. All calls
+// share it and it keeps the last call's contents, so each call clears the
+// counters it uses first, on its own stream. Calls that overlap on the GPU
+// (other streams, threads or pools on the same device) race on it.
+#include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kv_launch.h"
+#include "kv_pool.h"
+#include "kv_pool_internal.h"
+
+namespace gtkv {
+namespace {
+
+constexpr int64_t kMaxPages = 65536;
+constexpr int kHeaderWords = 4;  // entries, n_seqs, max_pages, page-major flag
+constexpr int kMaxDevices = 128;
+
+// One counter per page, then the total. In host code this name is only a
+// stand-in for the array; kernels get its device address from counts_on().
+static __device__ __align__(256) int32_t g_plan_counts[kMaxPages + 1];
+
+int32_t* g_counts_addr[kMaxDevices] = {};
+std::mutex g_counts_mu;
+
+// Device address of g_plan_counts on `device`, which must be current. Looked
+// up on the first call per device and kept.
+cudaError_t counts_on(int device, int32_t** out) {
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_counts_mu);
+  if (g_counts_addr[device] == nullptr) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_plan_counts);
+    if (e != cudaSuccess) return e;
+    g_counts_addr[device] = static_cast<int32_t*>(ptr);
+  }
+  *out = g_counts_addr[device];
+  return cudaSuccess;
+}
+
+// Page bucket of entry e = s * max_pages + k, or -1 when the entry holds no
+// token of the sequence's window [start_s, len_s). Tombstones (negative
+// pages) read the page-0 sink; pages >= P are reported and left out.
+__device__ __forceinline__ int64_t page_of_entry(const DevPool& p, int64_t e, const int32_t* __restrict__ bt,
+                                                 int32_t max_pages, const int32_t* __restrict__ seq_start,
+                                                 const int32_t* __restrict__ seq_len, int& bits) {
+  const int64_t s = e / max_pages;
+  const int64_t k = e - s * max_pages;
+  int64_t lo = seq_start ? __ldg(seq_start + s) : 0;
+  if (lo < 0) lo = 0;
+  const int64_t hi = __ldg(seq_len + s);
+  if (k * p.ps >= hi || (k + 1) * p.ps <= lo) return -1;
+  const int64_t page = __ldg(bt + e);
+  if (page >= p.num_pages) {
+    bits |= KV_DEV_ERR_ROW;
+    return -1;
+  }
+  return page < 0 ? 0 : page;
+}
+
+__global__ void __launch_bounds__(kBlock) k_noalloc_count(DevPool p, const int32_t* __restrict__ bt,
+                                                          int64_t n_entries, int32_t max_pages,
+                                                          const int32_t* __restrict__ seq_start,
+                                                          const int32_t* __restrict__ seq_len, int32_t* counts) {
+  int bits = 0;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
+    const int64_t b = page_of_entry(p, e, bt, max_pages, seq_start, seq_len, bits);
+    if (b >= 0) atomicAdd(counts + b, 1);
+  }
+  if (bits) atomicOr(p.err, bits);
+}
+
+// Counts -> exclusive start offsets in place, one block of 1024 threads, each
+// owning a contiguous run of pages; writes the plan's header words.
+__global__ void __launch_bounds__(1024) k_noalloc_scan(int64_t n_pages, int32_t n_seqs, int32_t max_pages,
+                                                       int32_t* counts, int32_t* __restrict__ plan) {
+  __shared__ int32_t warp_total[32];
+  __shared__ int32_t pages_used;
+  const int t = threadIdx.x;
+  if (t == 0) pages_used = 0;
+  const int64_t per = (n_pages + blockDim.x - 1) / blockDim.x;
+  const int64_t first = t * per < n_pages ? t * per : n_pages;
+  const int64_t last = first + per < n_pages ? first + per : n_pages;
+  int32_t mine = 0, used = 0;
+  for (int64_t i = first; i < last; ++i) {
+    const int32_t c = counts[i];
+    mine += c;
+    used += c > 0;
+  }
+  __syncthreads();
+  if (used) atomicAdd(&pages_used, used);
+  const int lane = t & 31, warp = t >> 5;
+  int32_t upto = mine;  // inclusive prefix within the warp
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t v = __shfl_up_sync(kFull, upto, d);
+    if (lane >= d) upto += v;
+  }
+  if (lane == 31) warp_total[warp] = upto;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = lane < static_cast<int>(blockDim.x >> 5) ? warp_total[lane] : 0;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t v = __shfl_up_sync(kFull, w, d);
+      if (lane >= d) w += v;
+    }
+    warp_total[lane] = w;  // inclusive prefix over warps
+  }
+  __syncthreads();
+  int32_t at = upto - mine + (warp > 0 ? warp_total[warp - 1] : 0);
+  for (int64_t i = first; i < last; ++i) {
+    const int32_t c = counts[i];
+    counts[i] = at;
+    at += c;
+  }
+  if (t == static_cast<int>(blockDim.x) - 1) {
+    counts[n_pages] = at;
+    plan[0] = at;
+    plan[1] = n_seqs;
+    plan[2] = max_pages;
+    plan[3] = 2 * static_cast<int64_t>(at) >= 3 * static_cast<int64_t>(pages_used) ? 1 : 0;
+  }
+}
+
+// Each entry takes the next position of its page; afterwards counts[b] is the
+// end offset of page b, as in kv_gather_plan's plan.
+__global__ void __launch_bounds__(kBlock) k_noalloc_scatter(DevPool p, const int32_t* __restrict__ bt,
+                                                            int64_t n_entries, int32_t max_pages,
+                                                            const int32_t* __restrict__ seq_start,
+                                                            const int32_t* __restrict__ seq_len, int32_t* counts,
+                                                            int32_t* __restrict__ entries) {
+  int bits = 0;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
+    const int64_t b = page_of_entry(p, e, bt, max_pages, seq_start, seq_len, bits);
+    if (b >= 0) entries[atomicAdd(counts + b, 1)] = static_cast<int32_t>(e);
+  }
+}
+
+}  // namespace
+}  // namespace gtkv
+
+extern "C" int kv_gather_plan_noalloc(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs,
+                                      int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
+                                      void* plan_dev, int64_t plan_bytes, kv_stream_t stream) {
+  using namespace gtkv;
+  if (pool == nullptr) return KV_ERR_INVALID;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return KV_ERR_CUDA;
+  if (device != pool->device) return KV_ERR_DEVICE;
+  int64_t need = 0;
+  int rc = kv_gather_plan_bytes(pool, n_seqs, max_pages, &need);
+  if (rc != KV_OK) return rc;
+  const int64_t n_pages = pool->dev.num_pages;
+  if (n_pages > kMaxPages) return KV_ERR_CAPACITY;
+  if (plan_dev == nullptr || plan_bytes < need) return KV_ERR_INVALID;
+  if (n_seqs > 0 && (seq_len_dev == nullptr || (block_table_dev == nullptr && max_pages > 0)))
+    return KV_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(plan_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_len_dev) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_start_dev) & 3u))
+    return KV_ERR_ALIGN;
+  int32_t* counts = nullptr;
+  if (counts_on(device, &counts) != cudaSuccess) return KV_ERR_CUDA;
+
+  nvtxRangePushA("kv_gather_plan_noalloc");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* plan = static_cast<int32_t*>(plan_dev);
+  const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
+  const size_t count_bytes = sizeof(int32_t) * static_cast<size_t>(n_pages + 1);
+  const unsigned grid = grid_for(k_noalloc_count, (n_entries + 31) / 32, pool->sm_count);
+  cudaError_t e = cudaMemsetAsync(counts, 0, count_bytes, s);  // the last call's counts are still there
+  if (e == cudaSuccess) {
+    k_noalloc_count<<<grid, kBlock, 0, s>>>(pool->dev, block_table_dev, n_entries, max_pages, seq_start_dev,
+                                            seq_len_dev, counts);
+    k_noalloc_scan<<<1, 1024, 0, s>>>(n_pages, n_seqs, max_pages, counts, plan);
+    k_noalloc_scatter<<<grid, kBlock, 0, s>>>(pool->dev, block_table_dev, n_entries, max_pages, seq_start_dev,
+                                              seq_len_dev, counts, plan + kHeaderWords + n_pages + 1);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaMemcpyAsync(plan + kHeaderWords, counts, count_bytes, cudaMemcpyDeviceToDevice, s);
+  nvtxRangePop();
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}

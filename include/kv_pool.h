@@ -69,7 +69,8 @@ enum {
   KV_ERR_TAIL_PAD = -4,   /* raw buffer ends before the last view does */
   KV_ERR_ALIGN = -5,      /* a pointer, the anchor or the row size breaks 16-byte alignment */
   KV_ERR_CUDA = -6,       /* a CUDA runtime call or a kernel launch failed */
-  KV_ERR_DEVICE = -7      /* called with a current device other than the pool's */
+  KV_ERR_DEVICE = -7,     /* called with a current device other than the pool's */
+  KV_ERR_CAPACITY = -8    /* more pages than kv_gather_plan_noalloc's fixed workspace holds */
 };
 
 /* Bits of the device error word (kv_pool_last_error). */
@@ -295,6 +296,36 @@ int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* pl
                             const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
                             const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
                             void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream);
+
+/* kv_gather_plan without any device memory from the caller beyond the plan.
+ * The paper has no counterpart: this entry point exists for callers of this
+ * library that cannot call cudaMalloc, such as code running inside a host
+ * framework whose allocator reserved the device's memory up front and owns
+ * it, or a serving loop that must not let an allocation (or the device-wide
+ * synchronization a cudaMalloc or cudaFree may bring) into its steady state.
+ * kv_gather_plan counts entries per page in the plan buffer itself; this
+ * variant counts in a fixed array inside the library's device image and then
+ * copies the resulting per-page offsets into the plan.
+ *
+ * Arguments, plan layout and device error bits are those of kv_gather_plan,
+ * and plan_bytes must still be at least kv_gather_plan_bytes(). The plan
+ * written is kv_gather_plan's up to the order of entries within one page
+ * (that order is not fixed in either), and kv_gather_layer_planned takes it
+ * unchanged. Calls no cudaMalloc or cudaFree and allocates nothing.
+ *
+ * Limit: pools of at most 65536 pages; larger pools return KV_ERR_CAPACITY
+ * before anything is enqueued. The array (65537 int32 counters, 256 KiB + 4 B)
+ * is held by every GPU that loads the library until the process exits.
+ * Set-up: the first call on each device looks up the array's device address
+ * with that device current (cudaGetSymbolAddress); make that first call
+ * before any stream capture. Sharing: every call uses the same array, which
+ * keeps the previous call's contents; each call clears the counters it uses
+ * on its stream first, so calls ordered on the GPU are independent, but calls
+ * that overlap on the GPU (different streams, threads or pools on one device)
+ * race on the array and give wrong plans: order them. */
+int kv_gather_plan_noalloc(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs,
+                           int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
+                           void* plan_dev, int64_t plan_bytes, kv_stream_t stream);
 
 /* Move: copy every row-block (all layers' K and V, 2L rows) of token
  * src_ids[i] to token dst_ids[i].
