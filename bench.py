@@ -446,7 +446,11 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": "kv_gather_layer_planned", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": gather_bytes, "avg_launch_ms": round(gather_ms, 4)},
+                     "algorithmic_bytes_per_launch": gather_bytes, "avg_launch_ms": round(gather_ms, 4),
+                     # useful bytes count a shared page once per reader; DRAM moves it about once
+                     # (L2 serves the rest), so the DRAM-side rate is the one bounded by the peak
+                     "dram_achieved": None if traffic is None else round(traffic / (gather_ms * 1e-3) / GB, 1),
+                     "dram_frac": None if traffic is None else round(traffic / (gather_ms * 1e-3) / GB / peak, 4)},
         "e2e": {"value": round(whole_job_gbps(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
