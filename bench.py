@@ -501,7 +501,7 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ per-kernel table
 
-MICRO_DEFAULT = ["translate:2", "block_table:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2",
+MICRO_DEFAULT = ["ceiling:0", "translate:2", "block_table:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2",
                  "gather_planned:2", "move:2",
                  "translate:3", "store:3", "store_slots:3", "store_all:3", "gather:3", "gather_planned:3",
                  "store:4", "gather:4", "gather_planned:4", "move:4",
@@ -587,6 +587,27 @@ def run_micro(args):
             line["speedup_vs_torch_indexing"] = round(r / med, 2)
         line.update(extra or {})
         print(json.dumps(line), flush=True)
+
+    if "ceiling" in by_cfg.pop(0, []):
+        # context for the HBM-bound kernels: torch's own fill, copy and
+        # reduction over 4 GiB (library kernels, not part of the path), i.e.
+        # what a write-only, a copy and a read-only stream reach on this GPU
+        nb = 4 << 30
+        a = torch.empty(nb, dtype=torch.uint8, device=dev)
+        b = torch.empty(nb, dtype=torch.uint8, device=dev)
+        a.fill_(1)
+        w = a.view(torch.int32)
+        b64 = b.view(torch.int64)
+        ms = timed(lambda i: b64.fill_(i), args.iters, False)
+        report("ceiling_write", 0, "4 GiB, torch fill_ of int64 (write only)", ms, nb, nb // 16)
+        ms = timed(lambda i: b.zero_(), args.iters, False)
+        report("ceiling_write_zero", 0, "4 GiB, torch zero_ (write only)", ms, nb, nb // 16)
+        ms = timed(lambda i: b.copy_(a), args.iters, False)
+        report("ceiling_copy", 0, "4 GiB, torch copy_ (read + write)", ms, 2 * nb, nb // 16)
+        ms = timed(lambda i: w.amax(), args.iters, False)
+        report("ceiling_read", 0, "4 GiB, torch amax (read only)", ms, nb, nb // 16)
+        del a, b, w, b64
+        torch.cuda.empty_cache()
 
     for cfg, kernels in sorted(by_cfg.items()):
         sh = synth.SHAPES[cfg]

@@ -13,8 +13,9 @@
 // a run of consecutive pool rows (one page's block 2l, then the same run in
 // block 2l+1 for V) that lands on consecutive output rows cu_out[s] + j -
 // start_s. So the gather is a set of contiguous copies: each run is cut into
-// chunks of about 4 KiB, a warp takes one chunk at a time and copies its K
-// and V bytes as 16-byte vectors, all loads issued before the stores. No
+// chunks of about 4 KiB; a warp works out the runs of up to 8 consecutive
+// chunks at once (one per lane), then copies them in turn, K and V bytes as 16-byte
+// vectors, all loads of a round issued before its stores. No
 // search and no host synchronization: the item space is n_seqs x max_pages x
 // chunks_per_page, and an entry outside a sequence's window is an empty item.
 #include "kv_launch.h"
@@ -25,6 +26,9 @@ namespace {
 
 #ifndef GTKV_GATHER_CHUNK
 #define GTKV_GATHER_CHUNK 4096  // bytes of K (and of V) one warp copies per item
+#endif
+#ifndef GTKV_GATHER_MAX_BATCH
+#define GTKV_GATHER_MAX_BATCH 8  // consecutive items a warp takes at once (1..32)
 #endif
 
 // Metadata checks, one sequence per thread, grid-stride (they never gate the
@@ -102,8 +106,9 @@ __device__ __forceinline__ Run gather_item(const DevPool& p, int64_t sk, int64_t
 
 // Items = (table entry sk, chunk c), taken in table order, or in the order of
 // a page-major plan (PLANNED: kv_plan.cu). CHV 16-byte vectors per lane per
-// round: one round moves 32*CHV vectors of K and as many of V.
-template <int CHV, bool PLANNED>
+// round: one round moves 32*CHV vectors of K and, with HAS_V, as many of V
+// (a latent-only pool has no V rows).
+template <int CHV, bool PLANNED, bool HAS_V>
 __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer, const int32_t* __restrict__ bt,
                                                         int32_t n_seqs, int32_t max_pages,
                                                         const int32_t* __restrict__ seq_start,
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
                                                         const int64_t* __restrict__ cu, uint4* __restrict__ out_k,
                                                         uint4* __restrict__ out_v, int64_t out_rows,
                                                         int32_t chunk_rows, int32_t chunks_per_page,
-                                                        const int32_t* __restrict__ plan) {
+                                                        const int32_t* __restrict__ plan, int batch) {
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   check_gather_meta(p, n_seqs, max_pages, seq_start, seq_len, cu, out_rows, tid, nthreads);
@@ -137,53 +142,70 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
   const int64_t vpr = p.vpr;
   const int64_t ps_vec = p.ps * vpr;                                      // K -> V distance, in vectors
   const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * p.ps;  // K (or latent) block of the layer
-  const bool has_v = p.kv_rows == 2;
+  constexpr bool has_v = HAS_V;
   const int64_t n_items = n_units * chunks_per_page;
   const L2Policy pol = make_l2_policy();
 
-  for (int64_t it = tid >> 5; it < n_items; it += nthreads >> 5) {
-    const int64_t u = it / chunks_per_page;
-    const int64_t c = it - u * chunks_per_page;
-    int64_t sk = u;
-    if (PLANNED && order != nullptr) {
-      sk = __ldg(order + u);
-      if (sk < 0 || sk >= n_entries) {
-        if (lane == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
-        continue;
+  // A warp takes `batch` consecutive items at a time (8 chunks of 4 KiB: a
+  // whole 16-token entry of 2 KiB rows, read and written as one stream) and
+  // works their runs out at once: lane j takes
+  // item it0 + j (its plan position, table entry, window and output rows: a
+  // chain of dependent loads), so one chain's latency serves the whole batch;
+  // the warp then copies the runs in turn, each broadcast by shuffle.
+  const int64_t n_warps = nthreads >> 5;
+  for (int64_t it0 = (tid >> 5) * batch; it0 < n_items; it0 += n_warps * batch) {
+    Run mine{0, 0, 0, 0};
+    const int64_t it = it0 + lane;
+    if (lane < batch && it < n_items) {
+      const int64_t u = it / chunks_per_page;
+      const int64_t c = it - u * chunks_per_page;
+      int64_t sk = u;
+      bool ok = true;
+      if (PLANNED && order != nullptr) {
+        sk = __ldg(order + u);
+        if (sk < 0 || sk >= n_entries) {
+          atomicOr(p.err, KV_DEV_ERR_TABLE);
+          ok = false;
+        }
       }
+      if (ok) mine = gather_item(p, sk, c, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows, true);
     }
-    const Run r = gather_item(p, sk, c, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows,
-                              lane == 0);
-    if (r.kind == 0) continue;
-    uint4* dk = out_k + r.row * vpr;
-    uint4* dv = has_v ? out_v + r.row * vpr : nullptr;
-    const uint4* srck = p.base + r.src;
-    const uint4* srcv = srck + ps_vec;
-    if (r.kind == 1) {
-      for (int64_t v0 = 0; v0 < r.nvec; v0 += 32 * CHV) {
-        uint4 bk[CHV], bv[CHV];
+    const int nb = n_items - it0 < batch ? static_cast<int>(n_items - it0) : batch;
+    for (int j = 0; j < nb; ++j) {
+      const int kind = __shfl_sync(kFull, mine.kind, j);
+      if (kind == 0) continue;
+      const int64_t row = __shfl_sync(kFull, mine.row, j);
+      const int64_t nvec = __shfl_sync(kFull, mine.nvec, j);
+      const uint4* srck = p.base + __shfl_sync(kFull, mine.src, j);
+      const uint4* srcv = srck + ps_vec;
+      uint4* dk = out_k + row * vpr;
+      uint4* dv = has_v ? out_v + row * vpr : nullptr;
+      if (kind == 1) {
+        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * CHV) {
+          uint4 bk[CHV], bv[CHV];
 #pragma unroll
-        for (int i = 0; i < CHV; ++i) {
-          const int64_t v = v0 + lane + 32 * i;
-          if (v < r.nvec) {
-            bk[i] = ld16<GTKV_GATHER_LD>(srck + v, pol);
-            if (has_v) bv[i] = ld16<GTKV_GATHER_LD>(srcv + v, pol);
+          for (int i = 0; i < CHV; ++i) {
+            const int64_t v = v0 + lane + 32 * i;
+            if (v < nvec) {
+              bk[i] = ld16<GTKV_GATHER_LD>(srck + v, pol);
+              if (has_v) bv[i] = ld16<GTKV_GATHER_LD>(srcv + v, pol);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < CHV; ++i) {
+            const int64_t v = v0 + lane + 32 * i;
+            if (v < nvec) {
+              st16<GTKV_GATHER_ST>(dk + v, bk[i], pol);
+              if (has_v) st16<GTKV_GATHER_ST>(dv + v, bv[i], pol);
+            }
           }
         }
-#pragma unroll
-        for (int i = 0; i < CHV; ++i) {
-          const int64_t v = v0 + lane + 32 * i;
-          if (v < r.nvec) {
-            st16<GTKV_GATHER_ST>(dk + v, bk[i], pol);
-            if (has_v) st16<GTKV_GATHER_ST>(dv + v, bv[i], pol);
-          }
+      } else {  // tombstoned entry: every token of the run reads the page-0 sink row
+        for (int64_t v = lane; v < nvec; v += 32) {
+          const int64_t col = v % vpr;
+          st16<GTKV_GATHER_ST>(dk + v, ld16<GTKV_GATHER_LD>(srck + col, pol), pol);
+          if (has_v) st16<GTKV_GATHER_ST>(dv + v, ld16<GTKV_GATHER_LD>(srcv + col, pol), pol);
         }
-      }
-    } else {  // tombstoned entry: every token of the run reads the page-0 sink row
-      for (int64_t v = lane; v < r.nvec; v += 32) {
-        const int64_t col = v % vpr;
-        st16<GTKV_GATHER_ST>(dk + v, ld16<GTKV_GATHER_LD>(srck + col, pol), pol);
-        if (has_v) st16<GTKV_GATHER_ST>(dv + v, ld16<GTKV_GATHER_LD>(srcv + col, pol), pol);
       }
     }
   }
@@ -379,11 +401,18 @@ __global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
                           const int32_t* seq_start, const int32_t* seq_len, const int64_t* cu, void* out_k,
                           void* out_v, int64_t out_rows, const int32_t* plan, int sm_count, cudaStream_t s) {
-  constexpr int CHV = 8;  // one round = 32 lanes x 8 vectors = 4 KiB of K and 4 KiB of V in flight per warp
-  int64_t chunk_rows = GTKV_GATHER_CHUNK / (16 * p.vpr);
-  if (chunk_rows < 1) chunk_rows = 1;
-  if (chunk_rows > p.ps) chunk_rows = p.ps;
-  const int64_t cpp = (p.ps + chunk_rows - 1) / chunk_rows;
+  // rows per item: GTKV_GATHER_CHUNK bytes of K (and as many of V); a
+  // latent-only pool has no V, so its items take twice the K bytes and keep
+  // the same bytes in flight per warp
+  const bool latent = p.kv_rows == 1;
+  auto rows_per_item = [&](int64_t bytes) {
+    int64_t r = bytes / (16 * p.vpr);
+    if (r < 1) r = 1;
+    if (r > p.ps) r = p.ps;
+    return r;
+  };
+  int64_t chunk_rows = rows_per_item(GTKV_GATHER_CHUNK);
+  int64_t cpp = (p.ps + chunk_rows - 1) / chunk_rows;
   if (GTKV_GATHER_BULK && plan == nullptr && chunk_rows * 16 * p.vpr <= kBulkHalf) {
     constexpr int threads = 32 * GTKV_BULK_WARPS;
     constexpr size_t smem = static_cast<size_t>(GTKV_BULK_WARPS) * GTKV_BULK_STAGES * (kBulkStage + 8);
@@ -406,14 +435,28 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
         static_cast<uint4*>(out_v), out_rows, static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp));
     return cudaGetLastError();
   }
-  auto kernel = plan ? k_gather_runs<CHV, true> : k_gather_runs<CHV, false>;
+  // one round: 32 lanes x 8 vectors = 4 KiB of K and 4 KiB of V (latent: 8 KiB of K) in flight per warp
+  auto kernel = latent ? (plan ? k_gather_runs<16, true, false> : k_gather_runs<16, false, false>)
+                       : (plan ? k_gather_runs<8, true, true> : k_gather_runs<8, false, true>);
+  if (latent) {
+    chunk_rows = rows_per_item(2 * GTKV_GATHER_CHUNK);
+    cpp = (p.ps + chunk_rows - 1) / chunk_rows;
+  }
   int64_t warps = static_cast<int64_t>(n_seqs) * max_pages * cpp;
   const int64_t seq_warps = (static_cast<int64_t>(n_seqs) + 31) / 32;
   if (warps < seq_warps) warps = seq_warps;
   const unsigned grid = grid_for(kernel, warps, sm_count);
+  // items per warp batch: up to GTKV_GATHER_MAX_BATCH, fewer when the grid's
+  // warps would not all get a full batch
+  const int64_t grid_warps = static_cast<int64_t>(grid) * (kBlock / 32);
+  const int64_t n_items = static_cast<int64_t>(n_seqs) * max_pages * cpp;
+  int64_t batch = (n_items + grid_warps - 1) / grid_warps;
+  if (batch > GTKV_GATHER_MAX_BATCH) batch = GTKV_GATHER_MAX_BATCH;
+  if (batch < 1) batch = 1;
   kernel<<<grid, kBlock, 0, s>>>(p, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu,
                                  static_cast<uint4*>(out_k), static_cast<uint4*>(out_v), out_rows,
-                                 static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp), plan);
+                                 static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp), plan,
+                                 static_cast<int>(batch));
   return cudaGetLastError();
 }
 
