@@ -276,17 +276,32 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+template <bool PLANNED>
 __global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
     DevPool p, int32_t layer, const int32_t* __restrict__ bt, int32_t n_seqs, int32_t max_pages,
     const int32_t* __restrict__ seq_start, const int32_t* __restrict__ seq_len, const int64_t* __restrict__ cu,
     uint4* __restrict__ out_k, uint4* __restrict__ out_v, int64_t out_rows, int32_t chunk_rows,
-    int32_t chunks_per_page) {
+    int32_t chunks_per_page, const int32_t* __restrict__ plan, int batch) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int D = GTKV_BULK_STAGES;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t ps = p.ps;
   check_gather_meta(p, n_seqs, max_pages, seq_start, seq_len, cu, out_rows, tid, nthreads);
+  const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
+  int64_t n_units = n_entries;  // entries (table order) or plan positions, as in k_gather_runs
+  const int32_t* order = nullptr;
+  if constexpr (PLANNED) {
+    if (__ldg(plan + 1) != n_seqs || __ldg(plan + 2) != max_pages) {
+      if (tid == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
+      return;
+    }
+    if (__ldg(plan + 3) != 0) {
+      const int64_t np = __ldg(plan);
+      n_units = np < 0 ? 0 : (np > n_entries ? n_entries : np);
+      order = plan + 4 + p.num_pages + 1;
+    }
+  }
 
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
@@ -302,7 +317,7 @@ __global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
   const int64_t vpr = p.vpr;
   const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * ps;
   const bool has_v = p.kv_rows == 2;
-  const int64_t n_items = static_cast<int64_t>(n_seqs) * max_pages * chunks_per_page;
+  const int64_t n_items = n_units * chunks_per_page;
   const int64_t it_step = nthreads >> 5;
   const L2Policy pol = make_l2_policy();
 
@@ -342,16 +357,27 @@ __global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
     return ok;
   };
 
-  for (int64_t base = tid >> 5; base < n_items && !failed; base += 32 * it_step) {
-    // lane k works out item base + k*step: empty, an error, a sink run, or a bulk run
-    const int64_t it = base + lane * it_step;
+  for (int64_t it0 = (tid >> 5) * batch; it0 < n_items && !failed; it0 += it_step * batch) {
+    // lane k < batch works out item it0 + k: empty, an error, a sink run, or a bulk run
+    const int64_t it = it0 + lane;
     int64_t src = -1, row = 0;
     uint32_t bytes = 0;
     bool sink = false;
-    if (it < n_items) {
-      const int64_t sk = it / chunks_per_page;
-      const Run r = gather_item(p, sk, it - sk * chunks_per_page, koff, bt, max_pages, seq_start, seq_len, cu,
-                                out_rows, chunk_rows, true);
+    if (lane < batch && it < n_items) {
+      const int64_t u = it / chunks_per_page;
+      int64_t sk = u;
+      bool ok = true;
+      if (PLANNED && order != nullptr) {
+        sk = __ldg(order + u);
+        if (sk < 0 || sk >= n_entries) {
+          atomicOr(p.err, KV_DEV_ERR_TABLE);
+          ok = false;
+        }
+      }
+      Run r{0, 0, 0, 0};
+      if (ok)
+        r = gather_item(p, sk, it - u * chunks_per_page, koff, bt, max_pages, seq_start, seq_len, cu, out_rows,
+                        chunk_rows, true);
       if (r.kind != 0) {
         src = r.src;
         row = r.row;
@@ -413,26 +439,31 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
   };
   int64_t chunk_rows = rows_per_item(GTKV_GATHER_CHUNK);
   int64_t cpp = (p.ps + chunk_rows - 1) / chunk_rows;
-  if (GTKV_GATHER_BULK && plan == nullptr && chunk_rows * 16 * p.vpr <= kBulkHalf) {
+  if (GTKV_GATHER_BULK && chunk_rows * 16 * p.vpr <= kBulkHalf) {
     constexpr int threads = 32 * GTKV_BULK_WARPS;
     constexpr size_t smem = static_cast<size_t>(GTKV_BULK_WARPS) * GTKV_BULK_STAGES * (kBulkStage + 8);
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(k_gather_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+    auto bulk = plan ? k_gather_bulk<true> : k_gather_bulk<false>;
+    static bool attr[2] = {false, false};
+    if (!attr[plan ? 1 : 0]) {
+      cudaError_t e = cudaFuncSetAttribute(bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
-      attr = true;
+      attr[plan ? 1 : 0] = true;
     }
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_gather_bulk, threads, smem) != cudaSuccess || nb < 1)
-      nb = 1;
-    int64_t blocks = (static_cast<int64_t>(n_seqs) * max_pages * cpp + GTKV_BULK_WARPS - 1) / GTKV_BULK_WARPS;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, bulk, threads, smem) != cudaSuccess || nb < 1) nb = 1;
+    const int64_t n_items = static_cast<int64_t>(n_seqs) * max_pages * cpp;
+    int64_t blocks = (n_items + GTKV_BULK_WARPS - 1) / GTKV_BULK_WARPS;
     const int64_t cap = static_cast<int64_t>(sm_count) * nb;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    k_gather_bulk<<<static_cast<unsigned>(blocks), threads, smem, s>>>(
+    const int64_t grid_warps = blocks * GTKV_BULK_WARPS;
+    int64_t batch = (n_items + grid_warps - 1) / grid_warps;
+    if (batch > GTKV_GATHER_MAX_BATCH) batch = GTKV_GATHER_MAX_BATCH;
+    if (batch < 1) batch = 1;
+    bulk<<<static_cast<unsigned>(blocks), threads, smem, s>>>(
         p, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu, static_cast<uint4*>(out_k),
-        static_cast<uint4*>(out_v), out_rows, static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp));
+        static_cast<uint4*>(out_v), out_rows, static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp), plan,
+        static_cast<int>(batch));
     return cudaGetLastError();
   }
   // one round: 32 lanes x 8 vectors = 4 KiB of K and 4 KiB of V (latent: 8 KiB of K) in flight per warp
