@@ -501,10 +501,10 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ per-kernel table
 
-MICRO_DEFAULT = ["ceiling:0", "translate:2", "block_table:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2", "gather:2",
-                 "gather_planned:2", "move:2",
+MICRO_DEFAULT = ["ceiling:0", "translate:2", "block_table:2", "store:2", "store_slots:2", "store_graph:2", "store_all:2",
+                 "gather:2", "gather_planned:2", "move:2",
                  "translate:3", "store:3", "store_slots:3", "store_all:3", "gather:3", "gather_planned:3",
-                 "store:4", "gather:4", "gather_planned:4", "move:4",
+                 "translate_mapped:4", "store:4", "gather:4", "gather_planned:4", "move:4",
                  "translate:5", "store:5", "store_slots:5", "gather:5", "gather_planned:5", "move:5",
                  "store:6", "store_all:6", "gather:6", "gather_planned:6", "move:6"]
 
@@ -647,6 +647,18 @@ def run_micro(args):
         if "translate" in kernels:
             ms = timed(lambda i: gt.kv_translate(pool, slots_d, ids), calls, True)
             report("translate", cfg, f"{n} slots", ms, n * 12, n)
+        if "translate_mapped" in kernels:
+            # a hybrid model's SWA layers: full-pool slots through a full -> SWA
+            # token map over 4x this pool's slots, a quarter of it cleared
+            rm = np.random.default_rng(5)
+            n_full = 4 * P * ps
+            tmap = rm.integers(0, P * ps, size=n_full).astype(np.int64)
+            tmap[rm.random(n_full) < 0.25] = -1
+            fslots = d(rm.integers(0, n_full, size=n).astype(np.int64))
+            tmap_d = d(tmap)
+            ms = timed(lambda i: gt.kv_translate_mapped(pool, fslots, ids, tmap_d), calls, True)
+            report("translate_mapped", cfg, f"{n} slots through a {n_full}-entry token map", ms, n * 20, n)
+            gt.kv_translate(pool, slots_d, ids)
         if "block_table" in kernels:
             gbt = synth.gather_batch(sh)
             vt = d(gbt.block_table)
@@ -723,8 +735,12 @@ def run_micro(args):
                 ms = timed(lambda i: gt.kv_gather_layer_planned(pool, layers[i % len(layers)], plan, bt, ln, cu, ok,
                                                                 ov, st), max(calls, len(layers)), flush)
                 msp = timed(lambda i: gt.kv_gather_plan(pool, bt, ln, st, plan=plan), calls, True)
+                extra = dict(share, plan_build_us=round(statistics.mean(msp) * 1e3, 2))
+                if P <= 65536:  # the allocation-free plan's fixed workspace
+                    msn = timed(lambda i: gt.kv_gather_plan_noalloc(pool, bt, ln, plan, st), calls, True)
+                    extra["plan_build_noalloc_us"] = round(statistics.mean(msn) * 1e3, 2)
                 report("gather_layer_planned", cfg, f"{gb.block_table.shape[0]} seqs, {rows} rows, page-major plan",
-                       ms, useful, rows, dict(share, plan_build_us=round(statistics.mean(msp) * 1e3, 2)))
+                       ms, useful, rows, extra)
             ms = None
             if "gather" in kernels:
                 ms = timed(lambda i: gt.kv_gather_layer(pool, layers[i % len(layers)], bt, ln, cu, ok, ov, st),

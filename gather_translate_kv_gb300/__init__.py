@@ -117,7 +117,7 @@ def lib():
         "kv_gather_plan_bytes": [vp, i32, i32, P(i64)],
         "kv_gather_plan": [vp, vp, i32, i32, vp, vp, vp, i64, vp],
         "kv_gather_plan_noalloc": [vp, vp, i32, i32, vp, vp, vp, i64, vp],
-        "kv_gather_layer_planned": [vp, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
+        "kv_gather_layer_planned": [vp, i32, vp, i64, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
         "kv_translate_block_table": [vp, vp, i32, i32, vp, vp, i64, vp, vp],
         "kv_pool_last_error": [vp, vp, P(i32)],
     }
@@ -344,7 +344,8 @@ def kv_gather_layer_planned(pool: KVPool, layer: int, plan: torch.Tensor, block_
     if ob % R != 0 or (out_v is not None and out_v.numel() * out_v.element_size() != ob):
         raise ValueError("out_k and out_v must be the same size, a whole number of rows")
     _check("kv_gather_layer_planned", lib().kv_gather_layer_planned(
-        pool.handle, layer, _dev(plan, "plan", torch.int32), _dev(block_table, "block_table", torch.int32),
+        pool.handle, layer, _dev(plan, "plan", torch.int32), plan.numel() * 4,
+        _dev(block_table, "block_table", torch.int32),
         n_seqs, max_pages, _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
         _dev(cu_out, "cu_out", torch.int64), _dev(out_k, "out_k"), _dev(out_v, "out_v"), ob // R, _stream(stream)))
 

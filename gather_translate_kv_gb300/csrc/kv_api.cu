@@ -320,12 +320,16 @@ int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_
                                            as_stream(stream)));
 }
 
-int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* plan_dev,
+int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* plan_dev, int64_t plan_bytes,
                             const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
                             const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
                             void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream) {
   Range nvtx("kv_gather_layer_planned");
   if (plan_dev == nullptr) return KV_ERR_INVALID;
+  int64_t need = 0;
+  const int rc = kv_gather_plan_bytes(pool, n_seqs, max_pages, &need);
+  if (rc != KV_OK) return rc;
+  if (plan_bytes < need) return KV_ERR_INVALID;  // the kernel reads up to `need` bytes of the plan
   return gather(pool, layer, plan_dev, block_table_dev, n_seqs, max_pages, seq_start_dev, seq_len_dev, cu_out_dev,
                 out_k_dev, out_v_dev, out_rows, stream);
 }

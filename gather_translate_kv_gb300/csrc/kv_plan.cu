@@ -21,35 +21,16 @@
 // the plan. A tombstoned entry (negative page) reads the sink on page 0 and
 // is grouped with page 0; a page >= P raises KV_DEV_ERR_ROW and is left out.
 #include "kv_launch.h"
+#include "kv_plan.cuh"
 
 namespace gtkv {
 
 namespace {
 
-constexpr int kPlanHeader = 4;
-
-// Page bucket of entry e, or -1 when it holds no token of the window.
-__device__ __forceinline__ int64_t plan_bucket(const DevPool& p, int64_t e, const int32_t* __restrict__ bt,
-                                               int32_t max_pages, const int32_t* __restrict__ seq_start,
-                                               const int32_t* __restrict__ seq_len, int& bits) {
-  const int64_t s = e / max_pages;
-  const int64_t k = e - s * max_pages;
-  int64_t a = seq_start ? __ldg(seq_start + s) : 0;
-  if (a < 0) a = 0;
-  const int64_t b = __ldg(seq_len + s);
-  if (k * p.ps >= b || (k + 1) * p.ps <= a) return -1;
-  const int64_t page = __ldg(bt + e);
-  if (page >= p.num_pages) {
-    bits |= KV_DEV_ERR_ROW;
-    return -1;
-  }
-  return page < 0 ? 0 : page;
-}
-
 __global__ void __launch_bounds__(kBlock) k_plan_count(DevPool p, const int32_t* __restrict__ bt, int64_t n_entries,
                                                        int32_t max_pages, const int32_t* __restrict__ seq_start,
                                                        const int32_t* __restrict__ seq_len, int32_t* __restrict__ plan) {
-  int32_t* counts = plan + kPlanHeader;
+  int32_t* counts = plan + kPlanHeaderWords;
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
@@ -59,56 +40,10 @@ __global__ void __launch_bounds__(kBlock) k_plan_count(DevPool p, const int32_t*
   if (bits) atomicOr(p.err, bits);
 }
 
-// Exclusive scan of the P counts into start offsets, one block of 1024
-// threads, each owning a contiguous segment; the total goes to the header.
-__global__ void __launch_bounds__(1024) k_plan_scan(int64_t n_buckets, int32_t n_seqs, int32_t max_pages,
-                                                    int32_t* __restrict__ plan) {
-  __shared__ int32_t warp_sums[32];
-  __shared__ int32_t used_pages;
-  int32_t* counts = plan + kPlanHeader;
-  const int t = threadIdx.x;
-  if (t == 0) used_pages = 0;
-  const int64_t seg = (n_buckets + blockDim.x - 1) / blockDim.x;
-  const int64_t lo = t * seg < n_buckets ? t * seg : n_buckets;
-  const int64_t hi = lo + seg < n_buckets ? lo + seg : n_buckets;
-  int32_t sum = 0, used = 0;
-  for (int64_t i = lo; i < hi; ++i) {
-    sum += counts[i];
-    used += counts[i] > 0;
-  }
-  __syncthreads();
-  if (used) atomicAdd(&used_pages, used);
-  // block-wide exclusive scan of the per-thread sums
-  const int lane = t & 31, w = t >> 5;
-  int32_t incl = sum;
-  for (int d = 1; d < 32; d <<= 1) {
-    const int32_t v = __shfl_up_sync(kFull, incl, d);
-    if (lane >= d) incl += v;
-  }
-  if (lane == 31) warp_sums[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int32_t ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
-    for (int d = 1; d < 32; d <<= 1) {
-      const int32_t v = __shfl_up_sync(kFull, ws, d);
-      if (lane >= d) ws += v;
-    }
-    warp_sums[lane] = ws;  // inclusive over warps
-  }
-  __syncthreads();
-  int32_t run = incl - sum + (w > 0 ? warp_sums[w - 1] : 0);  // exclusive prefix of this segment
-  for (int64_t i = lo; i < hi; ++i) {
-    const int32_t c = counts[i];
-    counts[i] = run;
-    run += c;
-  }
-  if (t == static_cast<int>(blockDim.x) - 1) {
-    counts[n_buckets] = run;  // == total
-    plan[0] = run;
-    plan[1] = n_seqs;
-    plan[2] = max_pages;
-    plan[3] = 2 * static_cast<int64_t>(run) >= 3 * static_cast<int64_t>(used_pages) ? 1 : 0;
-  }
+// Counts -> start offsets (in place) and the plan header.
+__global__ void __launch_bounds__(kScanThreads) k_plan_scan(int64_t n_buckets, int32_t n_seqs, int32_t max_pages,
+                                                            int32_t* __restrict__ plan) {
+  scan_plan_counts(plan + kPlanHeaderWords, n_buckets, n_seqs, max_pages, plan);
 }
 
 __global__ void __launch_bounds__(kBlock) k_plan_scatter(DevPool p, const int32_t* __restrict__ bt,
@@ -116,7 +51,7 @@ __global__ void __launch_bounds__(kBlock) k_plan_scatter(DevPool p, const int32_
                                                          const int32_t* __restrict__ seq_start,
                                                          const int32_t* __restrict__ seq_len,
                                                          int32_t* __restrict__ plan) {
-  int32_t* offs = plan + kPlanHeader;
+  int32_t* offs = plan + kPlanHeaderWords;
   int32_t* entries = offs + p.num_pages + 1;
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -130,19 +65,19 @@ __global__ void __launch_bounds__(kBlock) k_plan_scatter(DevPool p, const int32_
 }  // namespace
 
 int64_t plan_words(const DevPool& p, int32_t n_seqs, int32_t max_pages) {
-  return kPlanHeader + p.num_pages + 1 + static_cast<int64_t>(n_seqs) * max_pages;
+  return kPlanHeaderWords + p.num_pages + 1 + static_cast<int64_t>(n_seqs) * max_pages;
 }
 
 cudaError_t launch_gather_plan(const DevPool& p, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
                                const int32_t* seq_start, const int32_t* seq_len, int32_t* plan, int sm_count,
                                cudaStream_t s) {
   const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
-  cudaError_t e = cudaMemsetAsync(plan, 0, sizeof(int32_t) * (kPlanHeader + p.num_pages + 1), s);
+  cudaError_t e = cudaMemsetAsync(plan, 0, sizeof(int32_t) * (kPlanHeaderWords + p.num_pages + 1), s);
   if (e != cudaSuccess) return e;
   const unsigned grid = grid_for(k_plan_count, (n_entries + 31) / 32, sm_count);
   k_plan_count<<<grid, kBlock, 0, s>>>(p, bt, n_entries, max_pages, seq_start, seq_len, plan);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_plan_scan<<<1, 1024, 0, s>>>(p.num_pages, n_seqs, max_pages, plan);
+  k_plan_scan<<<1, kScanThreads, 0, s>>>(p.num_pages, n_seqs, max_pages, plan);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   k_plan_scatter<<<grid, kBlock, 0, s>>>(p, bt, n_entries, max_pages, seq_start, seq_len, plan);
   return cudaGetLastError();

@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "kv_launch.h"
+#include "kv_plan.cuh"
 #include "kv_pool.h"
 #include "kv_pool_internal.h"
 
@@ -30,7 +31,6 @@ namespace gtkv {
 namespace {
 
 constexpr int64_t kMaxPages = 65536;
-constexpr int kHeaderWords = 4;  // entries, n_seqs, max_pages, page-major flag
 constexpr int kMaxDevices = 128;
 
 // One counter per page, then the total. In host code this name is only a
@@ -55,26 +55,6 @@ cudaError_t counts_on(int device, int32_t** out) {
   return cudaSuccess;
 }
 
-// Page bucket of entry e = s * max_pages + k, or -1 when the entry holds no
-// token of the sequence's window [start_s, len_s). Tombstones (negative
-// pages) read the page-0 sink; pages >= P are reported and left out.
-__device__ __forceinline__ int64_t page_of_entry(const DevPool& p, int64_t e, const int32_t* __restrict__ bt,
-                                                 int32_t max_pages, const int32_t* __restrict__ seq_start,
-                                                 const int32_t* __restrict__ seq_len, int& bits) {
-  const int64_t s = e / max_pages;
-  const int64_t k = e - s * max_pages;
-  int64_t lo = seq_start ? __ldg(seq_start + s) : 0;
-  if (lo < 0) lo = 0;
-  const int64_t hi = __ldg(seq_len + s);
-  if (k * p.ps >= hi || (k + 1) * p.ps <= lo) return -1;
-  const int64_t page = __ldg(bt + e);
-  if (page >= p.num_pages) {
-    bits |= KV_DEV_ERR_ROW;
-    return -1;
-  }
-  return page < 0 ? 0 : page;
-}
-
 __global__ void __launch_bounds__(kBlock) k_noalloc_count(DevPool p, const int32_t* __restrict__ bt,
                                                           int64_t n_entries, int32_t max_pages,
                                                           const int32_t* __restrict__ seq_start,
@@ -82,61 +62,16 @@ __global__ void __launch_bounds__(kBlock) k_noalloc_count(DevPool p, const int32
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
-    const int64_t b = page_of_entry(p, e, bt, max_pages, seq_start, seq_len, bits);
+    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
     if (b >= 0) atomicAdd(counts + b, 1);
   }
   if (bits) atomicOr(p.err, bits);
 }
 
-// Counts -> exclusive start offsets in place, one block of 1024 threads, each
-// owning a contiguous run of pages; writes the plan's header words.
-__global__ void __launch_bounds__(1024) k_noalloc_scan(int64_t n_pages, int32_t n_seqs, int32_t max_pages,
-                                                       int32_t* counts, int32_t* __restrict__ plan) {
-  __shared__ int32_t warp_total[32];
-  __shared__ int32_t pages_used;
-  const int t = threadIdx.x;
-  if (t == 0) pages_used = 0;
-  const int64_t per = (n_pages + blockDim.x - 1) / blockDim.x;
-  const int64_t first = t * per < n_pages ? t * per : n_pages;
-  const int64_t last = first + per < n_pages ? first + per : n_pages;
-  int32_t mine = 0, used = 0;
-  for (int64_t i = first; i < last; ++i) {
-    const int32_t c = counts[i];
-    mine += c;
-    used += c > 0;
-  }
-  __syncthreads();
-  if (used) atomicAdd(&pages_used, used);
-  const int lane = t & 31, warp = t >> 5;
-  int32_t upto = mine;  // inclusive prefix within the warp
-  for (int d = 1; d < 32; d <<= 1) {
-    const int32_t v = __shfl_up_sync(kFull, upto, d);
-    if (lane >= d) upto += v;
-  }
-  if (lane == 31) warp_total[warp] = upto;
-  __syncthreads();
-  if (warp == 0) {
-    int32_t w = lane < static_cast<int>(blockDim.x >> 5) ? warp_total[lane] : 0;
-    for (int d = 1; d < 32; d <<= 1) {
-      const int32_t v = __shfl_up_sync(kFull, w, d);
-      if (lane >= d) w += v;
-    }
-    warp_total[lane] = w;  // inclusive prefix over warps
-  }
-  __syncthreads();
-  int32_t at = upto - mine + (warp > 0 ? warp_total[warp - 1] : 0);
-  for (int64_t i = first; i < last; ++i) {
-    const int32_t c = counts[i];
-    counts[i] = at;
-    at += c;
-  }
-  if (t == static_cast<int>(blockDim.x) - 1) {
-    counts[n_pages] = at;
-    plan[0] = at;
-    plan[1] = n_seqs;
-    plan[2] = max_pages;
-    plan[3] = 2 * static_cast<int64_t>(at) >= 3 * static_cast<int64_t>(pages_used) ? 1 : 0;
-  }
+// Counts -> start offsets (in place) and the plan header.
+__global__ void __launch_bounds__(kScanThreads) k_noalloc_scan(int64_t n_pages, int32_t n_seqs, int32_t max_pages,
+                                                               int32_t* counts, int32_t* __restrict__ plan) {
+  scan_plan_counts(counts, n_pages, n_seqs, max_pages, plan);
 }
 
 // Each entry takes the next position of its page; afterwards counts[b] is the
@@ -149,7 +84,7 @@ __global__ void __launch_bounds__(kBlock) k_noalloc_scatter(DevPool p, const int
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
-    const int64_t b = page_of_entry(p, e, bt, max_pages, seq_start, seq_len, bits);
+    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
     if (b >= 0) entries[atomicAdd(counts + b, 1)] = static_cast<int32_t>(e);
   }
 }
@@ -189,12 +124,12 @@ extern "C" int kv_gather_plan_noalloc(const kv_pool_t* pool, const int32_t* bloc
   if (e == cudaSuccess) {
     k_noalloc_count<<<grid, kBlock, 0, s>>>(pool->dev, block_table_dev, n_entries, max_pages, seq_start_dev,
                                             seq_len_dev, counts);
-    k_noalloc_scan<<<1, 1024, 0, s>>>(n_pages, n_seqs, max_pages, counts, plan);
+    k_noalloc_scan<<<1, kScanThreads, 0, s>>>(n_pages, n_seqs, max_pages, counts, plan);
     k_noalloc_scatter<<<grid, kBlock, 0, s>>>(pool->dev, block_table_dev, n_entries, max_pages, seq_start_dev,
-                                              seq_len_dev, counts, plan + kHeaderWords + n_pages + 1);
+                                              seq_len_dev, counts, plan + kPlanHeaderWords + n_pages + 1);
     e = cudaGetLastError();
   }
-  if (e == cudaSuccess) e = cudaMemcpyAsync(plan + kHeaderWords, counts, count_bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(plan + kPlanHeaderWords, counts, count_bytes, cudaMemcpyDeviceToDevice, s);
   nvtxRangePop();
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }

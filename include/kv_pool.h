@@ -285,14 +285,16 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
  *   Only entries holding tokens of [start_s, len_s) enter the plan; an entry
  *   naming a page >= num_pages sets KV_DEV_ERR_ROW and is left out.
  * kv_gather_layer_planned: kv_gather_layer with the same arguments plus the
- *   plan built from the same block table, starts and lengths; the output is
- *   identical. A plan built for another table shape sets KV_DEV_ERR_TABLE and
- *   writes nothing; plan entries are bounds-checked one by one. */
+ *   plan built from the same block table, starts and lengths (plan_bytes: the
+ *   size of its buffer, at least kv_gather_plan_bytes(), else KV_ERR_INVALID);
+ *   the output is identical. A plan built for another table shape sets
+ *   KV_DEV_ERR_TABLE and writes nothing; plan entries are bounds-checked one
+ *   by one, so a stale or foreign plan never reads outside its buffer. */
 int kv_gather_plan_bytes(const kv_pool_t* pool, int32_t n_seqs, int32_t max_pages, int64_t* plan_bytes);
 int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
                    const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,
                    kv_stream_t stream);
-int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* plan_dev,
+int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* plan_dev, int64_t plan_bytes,
                             const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
                             const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
                             void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream);

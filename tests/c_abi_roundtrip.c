@@ -4,7 +4,8 @@
  *
  *   c_abi_roundtrip        host-only checks: sizes and start-up gates
  *   c_abi_roundtrip gpu    + a translate -> store -> gather round trip on the
- *                          current device, with the library owning the pool
+ *                          current device, with the library owning the pool,
+ *                          and the same gather through a page-major plan
  *
  * Pool: 2 layers, 2 KV heads, head_dim 8, bf16 (R = 32 bytes), page size 4,
  * 64 pages. Exit status 0 = every check passed.
@@ -111,6 +112,28 @@ static int gpu_roundtrip(void) {
   for (int j = 0; j < N; ++j)
     if (ids[j] != table[j / 4] * 16 + j % 4) return fail("kernel id", ids[j]);
   if (memcmp(gk, k, sizeof k) != 0 || memcmp(gv, v, sizeof v) != 0) return fail("round trip bytes", 0);
+
+  /* the same gather through a page-major plan: 4 * (4 + 64 + 1 + 1 * 4) bytes */
+  int64_t plan_bytes = 0;
+  if ((rc = kv_gather_plan_bytes(pool, 1, PAGES, &plan_bytes)) != KV_OK || plan_bytes != 4 * (4 + 64 + 1 + 4))
+    return fail("plan bytes", rc);
+  void* d_plan;
+  if (cudaMalloc(&d_plan, (size_t)plan_bytes)) return fail("cudaMalloc plan", 0);
+  cudaMemset(d_gk, 0, sizeof gk);
+  cudaMemset(d_gv, 0, sizeof gv);
+  if ((rc = kv_gather_plan(pool, d_table, 1, PAGES, NULL, d_len, d_plan, plan_bytes, NULL)) != KV_OK)
+    return fail("plan", rc);
+  if ((rc = kv_gather_layer_planned(pool, 1, d_plan, plan_bytes - 4, d_table, 1, PAGES, NULL, d_len, d_cu, d_gk,
+                                    d_gv, N, NULL)) != KV_ERR_INVALID)
+    return fail("short plan buffer accepted", rc);
+  if ((rc = kv_gather_layer_planned(pool, 1, d_plan, plan_bytes, d_table, 1, PAGES, NULL, d_len, d_cu, d_gk, d_gv,
+                                    N, NULL)) != KV_OK)
+    return fail("planned gather", rc);
+  if ((rc = kv_pool_last_error(pool, NULL, &bits)) != KV_OK || bits != 0) return fail("device errors (plan)", bits);
+  cudaMemcpy(gk, d_gk, sizeof gk, cudaMemcpyDeviceToHost);
+  cudaMemcpy(gv, d_gv, sizeof gv, cudaMemcpyDeviceToHost);
+  if (memcmp(gk, k, sizeof k) != 0 || memcmp(gv, v, sizeof v) != 0) return fail("planned round trip bytes", 0);
+  cudaFree(d_plan);
   cudaFree(d_slots);
   cudaFree(d_ids);
   cudaFree(d_table);

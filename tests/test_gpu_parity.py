@@ -584,10 +584,15 @@ def test_planned_gather_matches_oracle(shape, anchor, latent):
         gt.kv_gather_layer_planned(pp.pool, 0, pd, to_dev(btd), to_dev(ln), to_dev(g.cu), dk, dv, to_dev(st))
         assert err == 0 and pp.last_error() == 0
         assert_bytes_equal(dk.cpu().numpy(), ok, "planned gather, table order", R)
-    # a plan built for another table shape is refused on the device, nothing written
-    other = gt.kv_gather_plan(pp.pool, to_dev(bt[:, :-1]), to_dev(np.minimum(ln, (maxp - 1) * ps)))
+    # a plan built for another table shape: a buffer too small for this table
+    # is refused on the host, a large enough one on the device; nothing written
     dk = torch.full((g.total, R), 0x33, dtype=torch.uint8, device="cuda")
     dv = None if latent else torch.full((g.total, R), 0x33, dtype=torch.uint8, device="cuda")
+    small = gt.kv_gather_plan(pp.pool, to_dev(bt[:, :-1]), to_dev(np.minimum(ln, (maxp - 1) * ps)))
+    with pytest.raises(gt.KVError) as e:
+        gt.kv_gather_layer_planned(pp.pool, 0, small, to_dev(bt), to_dev(ln), to_dev(g.cu), dk, dv, to_dev(st))
+    assert e.value.name == "KV_ERR_INVALID"
+    other = gt.kv_gather_plan(pp.pool, to_dev(np.concatenate([bt, bt])), to_dev(np.concatenate([ln, ln])))
     gt.kv_gather_layer_planned(pp.pool, 0, other, to_dev(bt), to_dev(ln), to_dev(g.cu), dk, dv, to_dev(st))
     assert pp.last_error() == gt.KV_DEV_ERR_TABLE
     assert bool((dk == 0x33).all())
