@@ -33,8 +33,9 @@
  *    owns every buffer it passes.
  *  - Compute calls are asynchronous on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream), launch only this library's kernels, allocate
- *    nothing and never synchronize, so they can be captured in a CUDA graph.
- *    kv_pool_last_error is the one call that synchronizes.
+ *    nothing and never synchronize; all but kv_gather_plan_noalloc (see its
+ *    own comment) can be captured in a CUDA graph. kv_pool_last_error is the
+ *    one call that synchronizes.
  *  - The calling thread's current device must be the pool's device.
  *  - Return value: KV_OK (0) or a negative KV_ERR_* code. These are argument,
  *    layout and launch errors, found on the host before anything is enqueued

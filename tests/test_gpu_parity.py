@@ -285,7 +285,8 @@ def test_gather_tombstoned_table_entry_reads_sink():
 
 
 def test_calls_capture_in_a_cuda_graph():
-    """translate -> store -> gather captured once, replayed on new inputs."""
+    """translate -> store -> gather, and plan -> planned gather, captured once,
+    replayed on new inputs."""
     shape = synth.SHAPES[2].scaled(24)
     pp = PoolPair(shape)
     o, R, ps, P = pp.o, pp.R, shape.page_size, shape.num_pages
@@ -300,21 +301,28 @@ def test_calls_capture_in_a_cuda_graph():
     bt_d, ln_d, cu_d = to_dev(bt), to_dev(g.seq_len), to_dev(g.cu)
     ok_d = torch.zeros((g.total, R), dtype=torch.uint8, device="cuda")
     ov_d = torch.zeros_like(ok_d)
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):  # warm-up outside capture
+    pk_d = torch.zeros_like(ok_d)
+    pv_d = torch.zeros_like(ok_d)
+    plan_d = torch.zeros(gt.kv_gather_plan_bytes(pp.pool, *bt.shape) // 4, dtype=torch.int32, device="cuda")
+
+    def step():
         gt.kv_translate(pp.pool, slots_d, ids_d)
         gt.kv_store_layer(pp.pool, 3, ids_d, k_d, v_d)
         gt.kv_gather_layer(pp.pool, 3, bt_d, ln_d, cu_d, ok_d, ov_d)
+        gt.kv_gather_plan(pp.pool, bt_d, ln_d, plan=plan_d)
+        gt.kv_gather_layer_planned(pp.pool, 3, plan_d, bt_d, ln_d, cu_d, pk_d, pv_d)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture
+        step()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     # restore the pool and the mirror to the sentinel before the replays
     synth.fill_sentinel_torch(pp.raw, pp.fill_seed)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        gt.kv_translate(pp.pool, slots_d, ids_d)
-        gt.kv_store_layer(pp.pool, 3, ids_d, k_d, v_d)
-        gt.kv_gather_layer(pp.pool, 3, bt_d, ln_d, cu_d, ok_d, ov_d)
+        step()
     rng = np.random.default_rng(9)
     for rep in range(2):
         slots = synth.distinct_slots(rng, ps, 17 * ps, n)  # pages the gather reads
@@ -328,6 +336,8 @@ def test_calls_capture_in_a_cuda_graph():
         rk, rv, _ = o.gather(pp.M, 3, bt, g.seq_len, g.cu)
         assert_bytes_equal(ok_d.cpu().numpy(), rk, "graph gather K", R)
         assert_bytes_equal(ov_d.cpu().numpy(), rv, "graph gather V", R)
+        assert_bytes_equal(pk_d.cpu().numpy(), rk, "graph planned gather K", R)
+        assert_bytes_equal(pv_d.cpu().numpy(), rv, "graph planned gather V", R)
         assert_pool_matches(pp, M0, {})
     assert pp.last_error() == 0
     pp.close()
