@@ -127,6 +127,8 @@ def lib(path: str | None = None):
         L.ora_block_table_kf.restype = ctypes.c_int
         L.ora_translate_mapped.argtypes = [P(_Desc), vp, c64, vp, c64, vp, c64, vp]
         L.ora_translate_mapped.restype = ctypes.c_int
+        L.ora_translate_multiplier.argtypes = [P(_Desc), vp, c64, c32, vp]
+        L.ora_translate_multiplier.restype = ctypes.c_int
         if path is not None:
             return L
         _lib = L
@@ -172,6 +174,15 @@ class Oracle:
         err = self._L.ora_translate(
             ctypes.byref(self._d), _ptr(slots), slots.size, _ptr(v), 0 if v is None else v.size, _ptr(ids)
         )
+        return ids, err
+
+    def translate_multiplier(self, slots: np.ndarray, multiplier: int):
+        """Test only: ids with an explicit kernel_page_multiplier (the library's is
+        always blocks_per_page); used to pin the multiplier-1 collapse."""
+        slots = np.ascontiguousarray(slots, dtype=np.int64)
+        ids = np.empty(slots.shape, dtype=np.int32)
+        err = self._L.ora_translate_multiplier(ctypes.byref(self._d), _ptr(slots), slots.size, int(multiplier),
+                                               _ptr(ids))
         return ids, err
 
     def translate_mapped(self, slots: np.ndarray, tmap: np.ndarray, v2p: np.ndarray | None = None):

@@ -212,6 +212,25 @@ int ora_translate(const ora_desc* d, const int64_t* slots, int64_t n,
     return err;
 }
 
+/* Test only: translate with an explicit kernel_page_multiplier m,
+ *     id = phys * (ps * m) + t % ps   (tombstones -> 0).
+ * The report keeps such an override solely so tests can pin the
+ * "multiplier-1 collapse" (评论区精华; 风险与影响 item 1): with m = 1 the ids
+ * are physical slot ids, and a dense per-layer view then puts block b of a
+ * token at view row id + b*ps, i.e. onto rows of other tokens, silently. The
+ * library has no such parameter: its multiplier is always blocks_per_page(). */
+int ora_translate_multiplier(const ora_desc* d, const int64_t* slots, int64_t n, int32_t m, int32_t* ids) {
+    int err = 0;
+    int64_t stride = (int64_t)d->page_size * m;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t p, o;
+        int sink;
+        err |= locate_slot(d, slots[i], NULL, 0, &p, &o, &sink);
+        ids[i] = (int32_t)(p * stride + o);
+    }
+    return err;
+}
+
 /* Byte offset in M of the row of (slot, block), or -1 when the slot is a
  * tombstone or an error (both land on the sink). Used by tests that check a
  * full-size run one sampled row at a time. */

@@ -467,10 +467,37 @@ def pin_swa_token_map(so):
     assert err == err2 == 0 and np.array_equal(ids, ref)
 
 
+def pin_multiplier_one_collapse(so):
+    """The "multiplier-1 collapse" the report's review pins with a test-only
+    override (评论区精华; 风险与影响 item 1): ids translated with
+    kernel_page_multiplier = 1 are physical slot ids, and the dense per-layer
+    views (block b of id at view row id + b*ps) then land block b >= 1 of a
+    token on rows of other tokens. With the multiplier blocks_per_page() = 2L
+    the ids are translate()'s and the rows tile the pool once."""
+    L, H, D, it, ps, P = 2, 2, 8, 2, 4, 8
+    o = _mk(so, _geom(L, H, D, it, ps, P, 0))
+    slots = np.arange(P * ps, dtype=np.int64)
+    good, err = o.translate_multiplier(slots, 2 * L)
+    ref, err2 = o.translate(slots)
+    assert err == err2 == 0 and np.array_equal(good, ref)
+    rows = [int(k) + b * ps for k in good for b in range(2 * L)]
+    assert sorted(rows) == list(range(P * 2 * L * ps))  # a bijection onto the pool's rows
+    bad, err = o.translate_multiplier(slots, 1)
+    assert err == 0 and np.array_equal(bad, slots)  # physical slot ids
+    rows1 = [int(k) + b * ps for k in bad for b in range(2 * L)]
+    assert len(set(rows1)) < len(rows1)  # rows alias
+    # the first token of page 1, layer 0 K (block 0), lands on page 0's first
+    # token's layer 0 V row (block 1): a store of one overwrites the other
+    assert int(bad[ps]) + 0 * ps == int(bad[0]) + 1 * ps
+    # and every row of the multiplier-1 id space stays inside the first
+    # P*ps + (2L-1)*ps rows: the upper pages of the pool are never addressed
+    assert max(rows1) == P * ps - 1 + (2 * L - 1) * ps < P * 2 * L * ps - 1
+
+
 PINS = [
     pin_translate_golden, pin_layout_table, pin_gates, pin_bijection, pin_store_vs_strided,
     pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors, pin_address_mode,
-    pin_block_table_kf, pin_mla, pin_swa_token_map,
+    pin_block_table_kf, pin_mla, pin_swa_token_map, pin_multiplier_one_collapse,
 ]
 
 
