@@ -93,7 +93,7 @@ cudaError_t launch_move(const DevPool& p, const int32_t* src, const int32_t* dst
     constexpr int U = U0 < G ? U0 : G;  // one wave set fits in a 32-task batch
     auto kernel = k_move<G, VPL, U>;
     const int batch = task_batch(kernel, n_tasks, (32 / G) * U, sm_count);
-    const unsigned grid = grid_for(kernel, (n_tasks + batch - 1) / batch, sm_count);
+    const unsigned grid = grid_all((n_tasks + batch - 1) / batch);
     kernel<<<grid, kBlock, 0, s>>>(p, src, dst, n_tasks, batch);
     return cudaGetLastError();
   });

@@ -170,7 +170,7 @@ cudaError_t launch(const DevPool& p, int32_t layer0, int32_t n_layers, const int
     constexpr int U = U0 < G ? U0 : G;
     auto kernel = k_store<G, VPL, U, SLOTS>;
     const int batch = task_batch(kernel, n_tasks, (32 / G) * U, sm_count);
-    const unsigned grid = grid_for(kernel, (n_tasks + batch - 1) / batch, sm_count);
+    const unsigned grid = grid_all((n_tasks + batch - 1) / batch);
     kernel<<<grid, kBlock, 0, s>>>(p, layer0, n, n_tasks, ids, slots, v2p, v2p_len, static_cast<const uint4*>(k),
                                    static_cast<const uint4*>(v), batch);
     return cudaGetLastError();
