@@ -293,6 +293,63 @@ def whole_job_gbps(bytes_per_rank_step: int, world: int, ms_per_step: float) -> 
 
 # ------------------------------------------------------------------ GPU arm
 
+class Step:
+    """The timed step's device state and launch sequence (see make_step)."""
+
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def make_step(gt, pool, inp, dev, stream) -> Step:
+    """Device buffers of one rank's inputs and the step that bench.py times:
+    translate -> all-layer store of the chunk -> gather plan -> 32 x (decode
+    store + planned gather) -> move, every call on `stream`. The move's ids
+    are kernel-facing, translated once here with the library. The gather
+    output buffers are shared by the layers (the last layer's rows remain).
+    Step.step(x, record) runs one step on the inputs x (Step.dev_in, or any
+    dict of device tensors of the same shapes); with record=True it appends
+    CUDA events around each gather to Step.gather_ev."""
+    import torch
+
+    L, R = SHAPE.layer_num, SHAPE.row_bytes
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    g = inp["g"]
+    dev_in = dict(slots=d(inp["slots"]), bt=d(g.block_table), ln=d(g.seq_len), cu=d(g.cu),
+                  k_dec=d(inp["k_dec"]), v_dec=d(inp["v_dec"]), k_chunk=d(inp["k_chunk"]),
+                  v_chunk=d(inp["v_chunk"]))
+    ids = torch.empty(N_DECODE + N_CHUNK, dtype=torch.int32, device=dev)
+    mv = torch.empty(2 * N_MOVE, dtype=torch.int32, device=dev)
+    gt.kv_translate(pool, d(np.concatenate([inp["move_src"], inp["move_dst"]])), mv, stream=stream)
+    mv_src, mv_dst = mv[:N_MOVE], mv[N_MOVE:]
+    out_k = torch.empty((g.total, R), dtype=torch.uint8, device=dev)
+    out_v = torch.empty_like(out_k)
+    plan = torch.empty(gt.kv_gather_plan_bytes(pool, *g.block_table.shape) // 4, dtype=torch.int32, device=dev)
+    gather_ev = []
+
+    def step(x, record=False):
+        gt.kv_translate(pool, x["slots"], ids, stream=stream)
+        gt.kv_store_all_layers(pool, ids[N_DECODE:], x["k_chunk"], x["v_chunk"], stream=stream)
+        gt.kv_gather_plan(pool, x["bt"], x["ln"], plan=plan, stream=stream)
+        for layer in range(L):
+            gt.kv_store_layer(pool, layer, ids[:N_DECODE], x["k_dec"][layer], x["v_dec"][layer], stream=stream)
+            if record:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            gt.kv_gather_layer_planned(pool, layer, plan, x["bt"], x["ln"], x["cu"], out_k, out_v, stream=stream)
+            if record:
+                e1.record(stream)
+                gather_ev.append((e0, e1))
+        gt.kv_move(pool, mv_src, mv_dst, stream=stream)
+
+    return Step(step=step, dev_in=dev_in, ids=ids, mv_src=mv_src, mv_dst=mv_dst, out_k=out_k, out_v=out_v,
+                plan=plan, gather_ev=gather_ev)
+
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -314,7 +371,7 @@ def run_gpu(args):
     gt.lib()
 
     sh = SHAPE
-    L, R, ps = sh.layer_num, sh.row_bytes, sh.page_size
+    L, ps = sh.layer_num, sh.page_size
     inp = make_inputs(rank)
     total, pad = gt.kv_pool_required_bytes(gt.make_desc(L, sh.head_num, sh.head_dim, sh.itemsize, ps,
                                                         sh.num_pages))
@@ -322,39 +379,9 @@ def run_gpu(args):
     synth.fill_sentinel_torch(raw, 17 + rank)
     pool = gt.kv_pool_create(gt.make_desc(L, sh.head_num, sh.head_dim, sh.itemsize, ps, sh.num_pages), raw)
 
-    def d(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    g = inp["g"]
-    dev_in = dict(slots=d(inp["slots"]), bt=d(g.block_table), ln=d(g.seq_len), cu=d(g.cu),
-                  k_dec=d(inp["k_dec"]), v_dec=d(inp["v_dec"]), k_chunk=d(inp["k_chunk"]),
-                  v_chunk=d(inp["v_chunk"]))
-    ids = torch.empty(N_DECODE + N_CHUNK, dtype=torch.int32, device=dev)
-    # move ids are kernel-facing: translate them once with the library
-    mv = torch.empty(2 * N_MOVE, dtype=torch.int32, device=dev)
-    gt.kv_translate(pool, d(np.concatenate([inp["move_src"], inp["move_dst"]])), mv)
-    mv_src, mv_dst = mv[:N_MOVE], mv[N_MOVE:]
-    out_k = torch.empty((g.total, R), dtype=torch.uint8, device=dev)
-    out_v = torch.empty_like(out_k)
-    plan = torch.empty(gt.kv_gather_plan_bytes(pool, *g.block_table.shape) // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    gather_ev = []
-
-    def step(x, record=False):
-        gt.kv_translate(pool, x["slots"], ids, stream=stream)
-        gt.kv_store_all_layers(pool, ids[N_DECODE:], x["k_chunk"], x["v_chunk"], stream=stream)
-        gt.kv_gather_plan(pool, x["bt"], x["ln"], plan=plan, stream=stream)
-        for layer in range(L):
-            gt.kv_store_layer(pool, layer, ids[:N_DECODE], x["k_dec"][layer], x["v_dec"][layer], stream=stream)
-            if record:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            gt.kv_gather_layer_planned(pool, layer, plan, x["bt"], x["ln"], x["cu"], out_k, out_v, stream=stream)
-            if record:
-                e1.record(stream)
-                gather_ev.append((e0, e1))
-        gt.kv_move(pool, mv_src, mv_dst, stream=stream)
+    st = make_step(gt, pool, inp, dev, stream)
+    step, dev_in, ids, gather_ev, g = st.step, st.dev_in, st.ids, st.gather_ev, inp["g"]
     launches_per_step = 1 + 1 + 3 + 2 * L + 1  # the plan is 3 kernels (+ a memset)
 
     for _ in range(args.warmup):

@@ -270,3 +270,65 @@ def test_id_bound_stress_full():
         F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]), planned=layer == 79)
     F.check_untouched()
     F.close()
+
+
+def test_bench_step_full():
+    """The step bench.py times, on its own inputs and in its own launch
+    configuration (bench.make_step on the full 8 GiB decode pool), run twice
+    as its warm-up does. Then the oracle's address mode checks every row the
+    step wrote or read: the 512 translated ids, the 256-token chunk and the
+    256 decode tokens in all 32 layers, every row of the last layer's planned
+    gather (256 x 4096 tokens; it reads rows the stores and the previous
+    step's move wrote), the 64 row-blocks of the 8192 moved tokens, and that
+    no other row of the pool changed."""
+    import bench
+
+    sh = bench.SHAPE
+    F = Full(sh)
+    inp = bench.make_inputs(0)
+    st = bench.make_step(gt, F.pool, inp, torch.device("cuda", torch.cuda.current_device()),
+                         torch.cuda.current_stream())
+    for _ in range(2):
+        st.step(st.dev_in)
+    torch.cuda.synchronize()
+    assert gt.kv_pool_last_error(F.pool) == 0
+    L, R = sh.layer_num, F.R
+
+    slots = inp["slots"]
+    ids_ref, err = F.o.translate(slots)
+    assert err == 0 and np.array_equal(st.ids.cpu().numpy(), ids_ref), "translated ids differ"
+
+    dec, chunk = slots[:bench.N_DECODE], slots[bench.N_DECODE:]
+    last_k, last_v = [], []
+    for layer in range(L):
+        for sl, kk, vv in ((chunk, inp["k_chunk"][layer], inp["v_chunk"][layer]),
+                           (dec, inp["k_dec"][layer], inp["v_dec"][layer])):
+            kd, vd, err = F.o.store_rows(layer, sl)
+            assert err == 0
+            Kd = torch.from_numpy(np.ascontiguousarray(kk)).cuda()
+            Vd = torch.from_numpy(np.ascontiguousarray(vv)).cuda()
+            F._check_rows(sl, kd, vd, Kd, Vd)
+            if layer == L - 1:
+                last_k.append((kd, Kd))
+                last_v.append((vd, Vd))
+
+    # the moved tokens' source rows were never written: they hold the sentinel
+    src_ids, e1 = F.o.translate(inp["move_src"])
+    dst_ids, e2 = F.o.translate(inp["move_dst"])
+    assert e1 == e2 == 0
+    sb, db, err = F.o.move_rows(src_ids, dst_ids)
+    assert err == 0
+    moved = F.sentinel(sb)
+    assert torch.equal(F.rows[torch.from_numpy(db // R).cuda()], moved), "moved rows differ"
+    F.written.append(torch.from_numpy(db // R).cuda())
+
+    # the gather buffers hold the last layer's rows; the second step's gather
+    # ran after the first step's move
+    g = inp["g"]
+    ks, vs, err = F.o.gather_rows(L - 1, g.block_table, g.seq_len, g.cu, g.seq_start)
+    assert err == 0 and (ks >= 0).all() and (vs >= 0).all()
+    assert torch.equal(st.out_k, F.expected_reads(ks, last_k + [(db, moved)])), "gathered K differs"
+    assert torch.equal(st.out_v, F.expected_reads(vs, last_v + [(db, moved)])), "gathered V differs"
+    del st
+    F.check_untouched()
+    F.close()
