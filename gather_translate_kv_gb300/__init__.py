@@ -149,6 +149,9 @@ def _dev(t: torch.Tensor | None, name: str, dtype=None, nbytes=None):
         return None
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # every call runs on the current device, which must be the pool's
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:

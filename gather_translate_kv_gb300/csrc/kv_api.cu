@@ -42,6 +42,14 @@ int enter(const kv_pool_t* pool) {
 
 int launched(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
 
+// The pool's device words: [0] the error word the kernels OR bits into,
+// [1] where kv_pool_last_error parks the value it took.
+constexpr size_t kErrWords = 2;
+
+// Read and clear the error word in one step, so a bit that work on another
+// stream raises meanwhile is kept for the next read instead of being lost.
+__global__ void k_take_error(int32_t* err) { err[1] = atomicExch(err, 0); }
+
 cudaStream_t as_stream(kv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 }  // namespace
@@ -88,6 +96,20 @@ int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, k
   if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return KV_ERR_CUDA;
+  if (raw_dev != nullptr) {
+    // a borrowed buffer must be device (or managed) memory of this device:
+    // anything else would only show up later, as a fault in a kernel
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, raw_dev) != cudaSuccess) {
+      cudaGetLastError();  // a failed query leaves its error for the next cudaGetLastError: clear it
+      return KV_ERR_INVALID;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+      if (a.device != dev) return KV_ERR_DEVICE;
+    } else {
+      return KV_ERR_INVALID;
+    }
+  }
 
   kv_pool* p = new (std::nothrow) kv_pool{};
   if (p == nullptr) return KV_ERR_INVALID;
@@ -110,7 +132,8 @@ int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, k
     p->owns_raw = 0;
   }
   void* err = nullptr;
-  if (cudaMalloc(&err, sizeof(int32_t)) != cudaSuccess || cudaMemset(err, 0, sizeof(int32_t)) != cudaSuccess) {
+  if (cudaMalloc(&err, kErrWords * sizeof(int32_t)) != cudaSuccess ||
+      cudaMemset(err, 0, kErrWords * sizeof(int32_t)) != cudaSuccess) {
     if (err) cudaFree(err);
     if (p->owns_raw) cudaFree(p->raw);
     delete p;
@@ -371,9 +394,10 @@ int kv_pool_last_error(const kv_pool_t* pool, kv_stream_t stream, int32_t* dev_c
   if (dev_code == nullptr) return KV_ERR_INVALID;
   int32_t h = 0;
   cudaStream_t s = as_stream(stream);
-  if (cudaMemcpyAsync(&h, pool->d_err, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KV_ERR_CUDA;
+  k_take_error<<<1, 1, 0, s>>>(pool->d_err);
+  if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaMemcpyAsync(&h, pool->d_err + 1, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KV_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ERR_CUDA;
-  if (cudaMemsetAsync(pool->d_err, 0, sizeof(int32_t), s) != cudaSuccess) return KV_ERR_CUDA;
   *dev_code = h;
   return KV_OK;
 }

@@ -57,9 +57,11 @@ __global__ void __launch_bounds__(kBlock) k_plan_scatter(DevPool p, const int32_
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
     const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
-    if (b >= 0) entries[atomicAdd(offs + b, 1)] = static_cast<int32_t>(e);
+    if (b >= 0) plan_place(entries, offs + b, n_entries, e, bits);
   }
-  // page >= P entries were already reported by the count pass
+  // page >= P entries were already reported by the count pass; a position
+  // past the plan means the table changed under the build
+  if (bits & KV_DEV_ERR_TABLE) atomicOr(p.err, KV_DEV_ERR_TABLE);
 }
 
 }  // namespace

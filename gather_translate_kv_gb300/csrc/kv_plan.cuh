@@ -30,6 +30,21 @@ __device__ __forceinline__ int64_t plan_bucket(const DevPool& p, int64_t e, cons
   return page < 0 ? 0 : page;
 }
 
+// Scatter step of the counting sort: entry e takes the next position of its
+// page's run. The positions come from the count pass over the same table, so
+// they stay below n_entries; if the table changed between the passes (a race
+// in the caller) a run could overflow, and such a position is dropped with
+// KV_DEV_ERR_TABLE instead of being written past the plan.
+__device__ __forceinline__ void plan_place(int32_t* __restrict__ entries, int32_t* next, int64_t n_entries, int64_t e,
+                                           int& bits) {
+  const int32_t pos = atomicAdd(next, 1);
+  if (pos >= 0 && pos < n_entries) {
+    entries[pos] = static_cast<int32_t>(e);
+  } else {
+    bits |= KV_DEV_ERR_TABLE;
+  }
+}
+
 constexpr int kScanThreads = 1024;
 constexpr int kScanPer = 4;                              // counters per thread per tile
 constexpr int kScanTile = kScanThreads * kScanPer;      // 4096 counters

@@ -70,14 +70,15 @@ enum {
   KV_ERR_TAIL_PAD = -4,   /* raw buffer ends before the last view does */
   KV_ERR_ALIGN = -5,      /* a pointer, the anchor or the row size breaks 16-byte alignment */
   KV_ERR_CUDA = -6,       /* a CUDA runtime call or a kernel launch failed */
-  KV_ERR_DEVICE = -7,     /* called with a current device other than the pool's */
+  KV_ERR_DEVICE = -7,     /* current device is not the pool's, or a buffer is another device's */
   KV_ERR_CAPACITY = -8    /* more pages than kv_gather_plan_noalloc's fixed workspace holds */
 };
 
 /* Bits of the device error word (kv_pool_last_error). */
 #define KV_DEV_ERR_ROW 1   /* an id / page addressed a row outside the pool; row skipped   */
 #define KV_DEV_ERR_V2P 2   /* translate: a virtual page index was past the page map        */
-#define KV_DEV_ERR_TABLE 4 /* gather: sequence metadata inconsistent (see kv_gather_layer) */
+#define KV_DEV_ERR_TABLE 4 /* gather: sequence metadata inconsistent (see kv_gather_layer);
+                              plan: the table changed while the plan was built */
 #define KV_DEV_ERR_FORM 8  /* move: an id was not p * ps * 2L + o with o < ps; pair skipped */
 #define KV_DEV_ERR_TIMEOUT 16 /* an asynchronous copy did not complete in time; the kernel stopped */
 
@@ -136,13 +137,15 @@ int kv_pool_required_bytes(const kv_pool_desc* desc, int64_t* total_bytes, int64
  *  raw_dev == NULL: the library allocates anchor + total + tail_pad bytes
  *    (cudaMalloc, contents undefined) and frees them in kv_pool_destroy.
  *  raw_dev != NULL: the pool borrows the caller's buffer (16-byte aligned,
- *    raw_bytes long) for its whole life; raw_bytes must reach
+ *    raw_bytes long, device or managed memory of the current device: host
+ *    memory gives KV_ERR_INVALID, another device's memory KV_ERR_DEVICE) for
+ *    its whole life; raw_bytes must reach
  *    last_view_end = anchor + (2L-1)*ps*R + n_rows*R, which build_mha_views
  *    asserts, else KV_ERR_TAIL_PAD. A buffer of anchor + total + tail_pad
  *    bytes always suffices.
  * Additionally requires R % 16 == 0 and anchor_bytes % 16 == 0
  * (KV_ERR_ALIGN): every kernel moves rows as 16-byte vectors.
- * Also allocates a 4-byte device error word. Launches no kernel.
+ * Also allocates the pool's device error word (8 bytes). Launches no kernel.
  * On success *out receives the handle; on failure *out is set to NULL and
  * nothing stays allocated. */
 int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, kv_pool_t** out);
@@ -284,7 +287,10 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
  *   With [3] = 0 (pages hardly shared) the planned gather keeps the table's
  *   own order, whose output writes stay sequential.
  *   Only entries holding tokens of [start_s, len_s) enter the plan; an entry
- *   naming a page >= num_pages sets KV_DEV_ERR_ROW and is left out.
+ *   naming a page >= num_pages sets KV_DEV_ERR_ROW and is left out. The
+ *   table must not change while the plan builds (it is read twice, to count
+ *   and to place); if it does, no write lands outside the plan, and an entry
+ *   without a place sets KV_DEV_ERR_TABLE.
  * kv_gather_layer_planned: kv_gather_layer with the same arguments plus the
  *   plan built from the same block table, starts and lengths (plan_bytes: the
  *   size of its buffer, at least kv_gather_plan_bytes(), else KV_ERR_INVALID);
@@ -364,10 +370,13 @@ int kv_translate_block_table(const kv_pool_t* pool, const int32_t* virt_bt_dev, 
                              const int32_t* seq_len_dev, const int32_t* v2p_dev, int64_t v2p_len,
                              int32_t* out_bt_dev, kv_stream_t stream);
 
-/* Read and clear the pool's device error word. Synchronizes `stream`, then
- * writes the KV_DEV_ERR_* bits raised since the last read into *dev_code and
- * zeroes the word (ordered on `stream`). Errors raised by work still running
- * on other streams may show up in a later read. */
+/* Read and clear the pool's device error word. Takes the word and zeroes it
+ * in one atomic exchange, ordered on `stream` (one tiny kernel), synchronizes
+ * `stream`, and writes the KV_DEV_ERR_* bits raised since the last read into
+ * *dev_code. Bits that work still running on other streams raises later stay
+ * in the word for the next read; none is lost. Two kv_pool_last_error calls
+ * on one pool must not overlap (they share the slot the taken value passes
+ * through). */
 int kv_pool_last_error(const kv_pool_t* pool, kv_stream_t stream, int32_t* dev_code);
 
 /* Name of a KV_OK / KV_ERR_* code (static string). */

@@ -268,6 +268,32 @@ def test_error_paths_match_oracle():
     pp.close()
 
 
+def test_create_rejects_a_buffer_that_is_not_device_memory():
+    """kv_pool_create checks where a borrowed buffer lives before any kernel
+    could touch it: host memory (pageable or pinned) is refused, device
+    memory of the current device is taken."""
+    import ctypes
+
+    desc = gt.make_desc(2, 2, 8, 2, 4, 64)
+    total, pad = gt.kv_pool_required_bytes(desc)
+    nbytes = total + pad
+    pageable = np.zeros(nbytes + 16, np.uint8)
+    base = pageable.ctypes.data
+    pinned = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    for ptr in (base + (-base) % 16, pinned.data_ptr()):
+        h = ctypes.c_void_p()
+        rc = gt.lib().kv_pool_create(ctypes.byref(desc), ctypes.c_void_p(ptr), nbytes, ctypes.byref(h))
+        assert gt.STATUS[rc] == "KV_ERR_INVALID" and not h.value
+    raw = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    pool = gt.kv_pool_create(desc, raw)
+    assert pool.info["raw_dev"] == raw.data_ptr() and pool.info["owns_raw"] == 0
+    # the refused calls left no CUDA error behind for the next launch to report
+    ids = torch.zeros(4, dtype=torch.int32, device="cuda")
+    gt.kv_translate(pool, torch.arange(4, 8, dtype=torch.int64, device="cuda"), ids)
+    assert gt.kv_pool_last_error(pool) == 0 and ids.tolist() == [16, 17, 18, 19]
+    gt.kv_pool_destroy(pool)
+
+
 def test_gather_tombstoned_table_entry_reads_sink():
     shape = S(0, "sink", 2, 2, 64, 2, 8, 10)
     pp = PoolPair(shape)
