@@ -294,6 +294,55 @@ def test_create_rejects_a_buffer_that_is_not_device_memory():
     gt.kv_pool_destroy(pool)
 
 
+def test_empty_calls_are_no_ops():
+    """Zero tokens, zero sequences, sequences without table entries and
+    zero-length sequences: every call returns KV_OK, raises no device error
+    bit, and changes no byte of the pool, of a gather output or of a block
+    table."""
+    shape = S(0, "empty", 2, 2, 64, 2, 4, 16)  # R=256
+    pp = PoolPair(shape)
+    M0 = pp.M.copy()
+    R, L = pp.R, shape.layer_num
+    i64 = torch.empty(0, dtype=torch.int64, device="cuda")
+    i32 = torch.empty(0, dtype=torch.int32, device="cuda")
+    rows0 = torch.empty((0, R), dtype=torch.uint8, device="cuda")
+    all0 = torch.empty((L, 0, R), dtype=torch.uint8, device="cuda")
+    gt.kv_translate(pp.pool, i64, i32)
+    gt.kv_translate_mapped(pp.pool, i64, i32, torch.zeros(8, dtype=torch.int64, device="cuda"))
+    gt.kv_store_layer(pp.pool, 1, i32, rows0, rows0)
+    gt.kv_store_all_layers(pp.pool, i32, all0, all0)
+    gt.kv_store_layer_slots(pp.pool, 0, i64, rows0, rows0)
+    gt.kv_store_all_layers_slots(pp.pool, i64, all0, all0)
+    gt.kv_move(pp.pool, i32, i32)
+    # no sequences at all
+    bt0 = torch.empty((0, 4), dtype=torch.int32, device="cuda")
+    cu0 = torch.zeros(1, dtype=torch.int64, device="cuda")
+    gt.kv_gather_layer(pp.pool, 0, bt0, i32, cu0, rows0, rows0)
+    plan0 = gt.kv_gather_plan(pp.pool, bt0, i32)
+    gt.kv_gather_layer_planned(pp.pool, 0, plan0, bt0, i32, cu0, rows0, rows0)
+    assert plan0[0].item() == 0
+    # three sequences with no table entries, and three zero-length sequences
+    # over a real table: nothing is read, no output row is written
+    zl = torch.zeros(3, dtype=torch.int32, device="cuda")
+    cu = torch.zeros(4, dtype=torch.int64, device="cuda")
+    gt.kv_gather_layer(pp.pool, 1, torch.empty((3, 0), dtype=torch.int32, device="cuda"), zl, cu, rows0, rows0)
+    bt = torch.tensor([[1, 2], [3, 4], [5, 6]], dtype=torch.int32, device="cuda")
+    ok = torch.full((5, R), 0x33, dtype=torch.uint8, device="cuda")
+    ov = torch.full((5, R), 0x44, dtype=torch.uint8, device="cuda")
+    gt.kv_gather_layer(pp.pool, 1, bt, zl, cu, ok, ov)
+    plan = gt.kv_gather_plan(pp.pool, bt, zl)
+    gt.kv_gather_layer_planned(pp.pool, 1, plan, bt, zl, cu, ok, ov)
+    assert plan[0].item() == 0
+    assert bool((ok == 0x33).all()) and bool((ov == 0x44).all())
+    # a prefix-only table translation of zero-length sequences touches no entry
+    v2p = torch.arange(16, dtype=torch.int32, device="cuda")
+    out = gt.kv_translate_block_table(pp.pool, bt, zl, v2p, out_bt=torch.full_like(bt, -9))
+    assert bool((out == -9).all())
+    assert pp.last_error() == 0
+    assert_pool_matches(pp, M0, {})
+    pp.close()
+
+
 def test_gather_tombstoned_table_entry_reads_sink():
     shape = S(0, "sink", 2, 2, 64, 2, 8, 10)
     pp = PoolPair(shape)
