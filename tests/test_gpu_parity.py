@@ -418,6 +418,136 @@ def test_calls_capture_in_a_cuda_graph():
     pp.close()
 
 
+def test_remaining_calls_capture_in_a_cuda_graph():
+    """The calls the graph test above leaves out, captured once with a page
+    map and replayed twice on new inputs: fused translate + all-layer store,
+    fused translate + per-layer store, translate of move ids, the move (of
+    tokens the same replay stored), the prefix-only kernel-facing block table
+    and the full -> SWA token map."""
+    shape = S(0, "graph2", 4, 2, 64, 2, 8, 40)  # R=256, L=4, ps=8
+    pp = PoolPair(shape)
+    o, R, L, ps, P = pp.o, pp.R, shape.layer_num, shape.page_size, shape.num_pages
+    M0 = pp.M.copy()
+    rng = np.random.default_rng(77)
+    v2p = np.zeros(P, np.int32)
+    v2p[1:] = 1 + rng.permutation(P - 1)  # a bijection of pages 1..P-1; page 0 stays the sink
+    na, nb, nm, S_, mp, nf, tlen = 48, 40, 16, 3, 4, 20, 300
+    z = lambda shp, dt: torch.zeros(shp, dtype=dt, device="cuda")  # noqa: E731
+    sa_d, sb_d = z(na, torch.int64), z(nb, torch.int64)
+    ka_d, va_d = z((L, na, R), torch.uint8), z((L, na, R), torch.uint8)
+    kb_d, vb_d = z((nb, R), torch.uint8), z((nb, R), torch.uint8)
+    ms_d, md_d = z(nm, torch.int64), z(nm, torch.int64)
+    src_d, dst_d = z(nm, torch.int32), z(nm, torch.int32)
+    vbt_d, ln_d, obt_d = z((S_, mp), torch.int32), z(S_, torch.int32), z((S_, mp), torch.int32)
+    fs_d, mid_d, tmap_d = z(nf, torch.int64), z(nf, torch.int32), z(tlen, torch.int64)
+    v2p_d = to_dev(v2p)
+
+    def step():
+        gt.kv_store_all_layers_slots(pp.pool, sa_d, ka_d, va_d, v2p=v2p_d)
+        gt.kv_store_layer_slots(pp.pool, 2, sb_d, kb_d, vb_d, v2p=v2p_d)
+        gt.kv_translate(pp.pool, ms_d, src_d, v2p_d)
+        gt.kv_translate(pp.pool, md_d, dst_d, v2p_d)
+        gt.kv_move(pp.pool, src_d, dst_d)
+        gt.kv_translate_block_table(pp.pool, vbt_d, ln_d, v2p_d, out_bt=obt_d)
+        gt.kv_translate_mapped(pp.pool, fs_d, mid_d, tmap_d, v2p=v2p_d)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture (all inputs zero: page-0 sink rows only)
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    synth.fill_sentinel_torch(pp.raw, pp.fill_seed)
+    assert pp.last_error() == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for rep in range(2):
+        sa = synth.distinct_slots(rng, ps, 13 * ps, na)           # virtual pages 1..12
+        sb = synth.distinct_slots(rng, 13 * ps, 20 * ps, nb)      # virtual pages 13..19
+        ms = rng.choice(sa, size=nm, replace=False)              # move tokens stored this replay
+        md = synth.distinct_slots(rng, 20 * ps, 30 * ps, nm)      # to virtual pages 20..29
+        Ka, Va = _vals(shape, rng, (L, na))
+        Kb, Vb = _vals(shape, rng, (nb,))
+        vbt = rng.integers(-1, P, size=(S_, mp)).astype(np.int32)
+        ln = rng.integers(0, mp * ps + 1, size=S_).astype(np.int32)
+        tmap = rng.integers(-1, P * ps, size=tlen).astype(np.int64)
+        fs = rng.integers(-2, tlen, size=nf).astype(np.int64)
+        for d, h in ((sa_d, sa), (sb_d, sb), (ms_d, ms), (md_d, md), (vbt_d, vbt), (ln_d, ln), (tmap_d, tmap),
+                     (fs_d, fs)):
+            d.copy_(to_dev(h))
+        ka_d.copy_(to_dev(as_rows(Ka, R).reshape(L, na, R)))
+        va_d.copy_(to_dev(as_rows(Va, R).reshape(L, na, R)))
+        kb_d.copy_(to_dev(as_rows(Kb, R)))
+        vb_d.copy_(to_dev(as_rows(Vb, R)))
+        obt_d.fill_(-7)
+        assert o.store_all(pp.M, sa, Ka, Va, v2p) == 0
+        assert o.store(pp.M, 2, sb, Kb, Vb, v2p) == 0
+        src, e1 = o.translate(ms, v2p)
+        dst, e2 = o.translate(md, v2p)
+        assert e1 == e2 == 0 and o.move(pp.M, src, dst) == 0
+        bt_ref, e3 = o.block_table_kf(vbt, ln, v2p)
+        mid_ref, e4 = o.translate_mapped(fs, tmap, v2p)
+        assert e3 == e4 == 0
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pp.last_error() == 0
+        assert np.array_equal(src_d.cpu().numpy(), src) and np.array_equal(dst_d.cpu().numpy(), dst)
+        assert np.array_equal(obt_d.cpu().numpy(), bt_ref), "graph block table"
+        assert np.array_equal(mid_d.cpu().numpy(), mid_ref), "graph token-mapped ids"
+        assert_pool_matches(pp, M0, {})
+    pp.close()
+
+
+def test_two_streams_share_one_pool():
+    """Two streams store and gather different layers of one pool at the same
+    time; one of them also stores a batch with an out-of-range id. Both
+    streams' results match the oracle and the error bit reaches the pool's
+    shared error word."""
+    shape = S(0, "streams", 4, 2, 64, 2, 8, 40)  # R=256, L=4, ps=8
+    pp = PoolPair(shape)
+    o, R, ps, P = pp.o, pp.R, shape.page_size, shape.num_pages
+    M0 = pp.M.copy()
+    rng = np.random.default_rng(78)
+    work = []
+    for layer, lo, hi in ((1, 1, 20), (3, 20, 40)):
+        slots = synth.distinct_slots(rng, lo * ps, hi * ps, 96)
+        K, V = _vals(shape, rng, (96,))
+        ids, _ = o.translate(slots)
+        bt = rng.integers(1, P, size=(6, 5)).astype(np.int32)
+        g = synth.GatherBatch(bt, np.zeros(6, np.int32), rng.integers(1, 5 * ps + 1, size=6).astype(np.int32))
+        work.append((layer, slots, K, V, ids, g))
+    bad = work[1][4].copy()
+    bad[7] = pp.sizes["n_rows"] + 3
+    dev = [dict(ids=to_dev(ids), K=to_dev(as_rows(K, R)), V=to_dev(as_rows(V, R)), bt=to_dev(g.block_table),
+                ln=to_dev(g.seq_len), cu=to_dev(g.cu), ok=torch.zeros((g.total, R), dtype=torch.uint8, device="cuda"),
+                ov=torch.zeros((g.total, R), dtype=torch.uint8, device="cuda"))
+           for (_, _, K, V, ids, g) in work]
+    bad_d = to_dev(bad)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    for (layer, *_), d, st in zip(work, dev, streams):
+        gt.kv_store_layer(pp.pool, layer, d["ids"], d["K"], d["V"], stream=st)
+        gt.kv_gather_layer(pp.pool, layer, d["bt"], d["ln"], d["cu"], d["ok"], d["ov"], stream=st)
+    # stream 2 then stores layer 0 with one id past the pool: that row is skipped
+    gt.kv_store_layer(pp.pool, 0, bad_d, dev[1]["K"], dev[1]["V"], stream=streams[1])
+    torch.cuda.synchronize()
+    assert pp.last_error() == gt.KV_DEV_ERR_ROW
+    for (layer, slots, K, V, ids, g), d in zip(work, dev):
+        assert o.store(pp.M, layer, slots, K, V) == 0
+        rk, rv, err = o.gather(pp.M, layer, g.block_table, g.seq_len, g.cu)
+        assert err == 0
+        assert_bytes_equal(d["ok"].cpu().numpy(), rk, f"stream gather K, layer {layer}", R)
+        assert_bytes_equal(d["ov"].cpu().numpy(), rv, f"stream gather V, layer {layer}", R)
+    keep = np.ones(96, bool)
+    keep[7] = False
+    _, slots1, K1, V1, _, _ = work[1]
+    assert o.store(pp.M, 0, slots1[keep], K1[keep], V1[keep]) == 0
+    assert_pool_matches(pp, M0, {})
+    pp.close()
+
+
 @pytest.mark.parametrize("shape,anchor", SHAPES[:6], ids=IDS[:6])
 def test_fused_translate_store_matches_oracle(shape, anchor):
     """kv_store_layer_slots / kv_store_all_layers_slots (translate fused into
