@@ -271,34 +271,4 @@ inline unsigned grid_for(K kernel, int64_t warps_needed, int sm_count) {
   return static_cast<unsigned>(blocks);
 }
 
-// Grid for `warps_needed` warps of work, one warp per batch of tasks and no
-// cap: the hardware block scheduler hands blocks to SMs as they free up, so
-// SMs whose memory traffic drains faster take more of the work. Used by the
-// store and the move. A persistent grid with a fixed share per warp
-// measured 4-10 % slower on them: on this GPU some SMs finish an equal share
-// of a write stream several times sooner than others, and the launch lasts
-// as long as the slowest.
-inline unsigned grid_all(int64_t warps_needed) {
-  const int64_t per_block = kBlock / 32;
-  int64_t blocks = (warps_needed + per_block - 1) / per_block;
-  if (blocks < 1) blocks = 1;
-  if (blocks > 0x7fffffff) blocks = 0x7fffffff;  // the kernels loop grid-stride beyond this
-  return static_cast<unsigned>(blocks);
-}
-
-// Tasks per warp batch for the row-task kernels (store, move): lanes hold the
-// metadata of up to 32 tasks, copied in waves of `wave` tasks. Large calls
-// take full 32-task batches; small ones shrink the batch (to a multiple of
-// the wave) so that the work still spreads over every SM.
-template <class K>
-inline int task_batch(K kernel, int64_t n_tasks, int wave, int sm_count) {
-  const int64_t warps_full = static_cast<int64_t>(sm_count) * blocks_per_sm(kernel) * (kBlock / 32);
-  int64_t b = (n_tasks + warps_full - 1) / warps_full;
-  if (wave > 32) wave = 32;
-  b = (b + wave - 1) / wave * wave;
-  if (b < wave) b = wave;
-  if (b > 32) b = 32 / wave * wave;
-  return static_cast<int>(b);
-}
-
 }  // namespace gtkv

@@ -9,6 +9,7 @@
 // Sources and destinations are disjoint by precondition, so loads use the
 // coherent path (the pool is written by this kernel) and need no ordering.
 #include "kv_launch.h"
+#include "kv_tasks.cuh"
 
 namespace gtkv {
 

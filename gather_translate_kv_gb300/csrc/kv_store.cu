@@ -11,6 +11,7 @@
 // (one latent row per layer, blocks_per_page = L) the row is id + l*ps and
 // there is no V.
 #include "kv_launch.h"
+#include "kv_tasks.cuh"
 
 namespace gtkv {
 
