@@ -3,7 +3,6 @@ include/kv_pool.h declares, and its layout gates agree with the oracle's.
 No compute call is made (no GPU here)."""
 import ctypes
 
-import numpy as np
 import pytest
 
 import gather_translate_kv_gb300 as gt
