@@ -289,10 +289,11 @@ class Oracle:
         return ks, vs, err
 
     def move_rows(self, src_ids, dst_ids):
-        """Byte offsets a move reads and writes: (src[m*2L], dst[m*2L], err)."""
+        """Byte offsets a move reads and writes: (src[m*B], dst[m*B], err), B the
+        row-blocks per page (2L, or L for an MLA pool)."""
         s = np.ascontiguousarray(src_ids, dtype=np.int32)
         d = np.ascontiguousarray(dst_ids, dtype=np.int32)
-        nb = 2 * self.geom.layer_num
+        nb = self.geom.blocks
         sb = np.empty(s.size * nb, np.int64)
         db = np.empty(s.size * nb, np.int64)
         err = self._L.ora_move_rows(ctypes.byref(self._d), _ptr(s), _ptr(d), s.size, _ptr(sb), _ptr(db))

@@ -19,6 +19,7 @@ models".
 """
 from __future__ import annotations
 
+import ctypes
 import os
 import sys
 
@@ -446,6 +447,61 @@ def pin_mla(so):
     assert np.array_equal(M, T)
 
 
+def pin_mla_address_mode(so):
+    """MLA pools in address mode (the form the full-size checks use): store,
+    gather and move name exactly the bytes their copying twins move, report
+    no V row, and a move names L rows per pair, one per layer (blocks_per_page()
+    returns layer_num for MLA, 实现拆解 step 2)."""
+    rng = np.random.default_rng(19)
+    L, H, D, it, ps, P = 4, 1, 32, 2, 8, 9
+    o = _mk(so, _geom(L, H, D, it, ps, P, latent=True))
+    R = o.sizes()["row_bytes"]
+    M = _fresh(o)
+    used = rng.permutation(np.arange(ps, P * ps))
+    slots = used[:20].astype(np.int64)
+    K = synth.kv_values(rng, (20, H, D), it)
+    T = M.copy()
+    assert o.store(M, 3, slots, K, None) == 0
+    kd, vd, err = o.store_rows(3, slots)
+    assert err == 0 and kd.size == 20 and np.all(vd == -1)
+    Kb = K.reshape(20, -1).view(np.uint8)
+    for i in range(20):
+        T[kd[i]:kd[i] + R] = Kb[i]
+    assert np.array_equal(M, T)
+    bt = rng.integers(1, P, size=(3, 4)).astype(np.int32)
+    gb = synth.GatherBatch(bt, np.array([0, 3, 9], np.int32), np.array([32, 20, 12], np.int32))
+    k, v, err = o.gather(M, 2, bt, gb.seq_len, gb.cu, gb.seq_start)
+    ks, vs, err2 = o.gather_rows(2, bt, gb.seq_len, gb.cu, gb.seq_start)
+    assert err == err2 == 0 and v is None and np.all(vs == -1)
+    for r in range(gb.total):
+        assert np.array_equal(k[r], M[ks[r]:ks[r] + R])
+    m = 6
+    src_slots, dst_slots = used[:m], used[20:20 + m]
+    src, _ = o.translate(src_slots)
+    dst, _ = o.translate(dst_slots)
+    # the raw routine first, into buffers twice the size it may write: it must
+    # fill exactly m * L entries and leave the rest alone
+    sb_raw = np.full(2 * m * L, -7, np.int64)
+    db_raw = np.full(2 * m * L, -7, np.int64)
+    err = o._L.ora_move_rows(ctypes.byref(o._d), src.ctypes.data, dst.ctypes.data, m, sb_raw.ctypes.data,
+                             db_raw.ctypes.data)
+    assert err == 0 and np.all(sb_raw[m * L:] == -7) and np.all(db_raw[m * L:] == -7)
+    sb, db, err = o.move_rows(src, dst)
+    assert err == 0 and sb.size == db.size == m * L
+    assert np.array_equal(sb, sb_raw[:m * L]) and np.array_equal(db, db_raw[:m * L])
+    # pair i, layer b names block b of the token, found by slot (not by id)
+    for i in range(m):
+        for b in range(L):
+            assert sb[i * L + b] == o.slot_row_byte(int(src_slots[i]), b)
+            assert db[i * L + b] == o.slot_row_byte(int(dst_slots[i]), b)
+    before = M.copy()
+    assert o.move(M, src, dst) == 0
+    T = before.copy()
+    for a, b in zip(sb, db):
+        T[b:b + R] = before[a:a + R]
+    assert np.array_equal(M, T)
+
+
 def pin_swa_token_map(so):
     """Full -> SWA token mapping (tests/golden/swa_map_tiny.txt), a slot past
     the map, and translate_mapped(t) = translate(map[t]) on random maps."""
@@ -497,7 +553,7 @@ def pin_multiplier_one_collapse(so):
 PINS = [
     pin_translate_golden, pin_layout_table, pin_gates, pin_bijection, pin_store_vs_strided,
     pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors, pin_address_mode,
-    pin_block_table_kf, pin_mla, pin_swa_token_map, pin_multiplier_one_collapse,
+    pin_block_table_kf, pin_mla, pin_mla_address_mode, pin_swa_token_map, pin_multiplier_one_collapse,
 ]
 
 

@@ -78,6 +78,9 @@ MUTANTS = [
     ("layer_stride_one_block",
      "int64_t page_bytes = (int64_t)d->page_size * blocks * R;",
      "int64_t page_bytes = (int64_t)d->page_size * (blocks - 1) * R;"),
+    ("mla_move_rows_names_2L_blocks",
+     "int64_t blocks = blocks_of(d);\n    int err = 0;\n    for (int64_t i = 0; i < m; ++i) {",
+     "int64_t blocks = 2 * (int64_t)d->layer_num;\n    int err = 0;\n    for (int64_t i = 0; i < m; ++i) {"),
     ("block_table_entry_not_scaled",
      "out[(int64_t)s * max_pages + k] = (int32_t)(phys < 0 ? 0 : phys * blocks);",
      "out[(int64_t)s * max_pages + k] = (int32_t)(phys < 0 ? 0 : phys);"),
