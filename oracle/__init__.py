@@ -115,6 +115,10 @@ def lib(path: str | None = None):
         L.ora_store_all.restype = ctypes.c_int
         L.ora_gather.argtypes = [P(_Desc), vp, c32, vp, c32, c32, vp, vp, vp, vp, vp, c64]
         L.ora_gather.restype = ctypes.c_int
+        L.ora_gather_kf.argtypes = [P(_Desc), vp, c32, vp, c32, c32, vp, vp, vp, vp, vp, c64]
+        L.ora_gather_kf.restype = ctypes.c_int
+        L.ora_gather_kf_rows.argtypes = [P(_Desc), c32, vp, c32, c32, vp, vp, vp, c64, vp, vp]
+        L.ora_gather_kf_rows.restype = ctypes.c_int
         L.ora_move.argtypes = [P(_Desc), vp, vp, vp, c64]
         L.ora_move.restype = ctypes.c_int
         L.ora_store_rows.argtypes = [P(_Desc), c32, vp, c64, vp, c64, vp, vp]
@@ -237,6 +241,17 @@ class Oracle:
     def gather(self, M, layer, block_table, seq_len, cu, seq_start=None, out_rows=None,
                outK=None, outV=None):
         """Returns (outK, outV, err) with outK/outV uint8 [out_rows, R]."""
+        return self._gather(self._L.ora_gather, M, layer, block_table, seq_len, cu, seq_start, out_rows, outK,
+                            outV)
+
+    def gather_kf(self, M, layer, kf_table, seq_len, cu, seq_start=None, out_rows=None,
+                  outK=None, outV=None):
+        """Gather through a kernel-facing block table (block_table_kf's output):
+        (outK, outV, err) as gather()."""
+        return self._gather(self._L.ora_gather_kf, M, layer, kf_table, seq_len, cu, seq_start, out_rows, outK,
+                            outV)
+
+    def _gather(self, fn, M, layer, block_table, seq_len, cu, seq_start, out_rows, outK, outV):
         bt = np.ascontiguousarray(block_table, dtype=np.int32)
         n_seqs, max_pages = bt.shape
         ln = np.ascontiguousarray(seq_len, dtype=np.int32)
@@ -249,10 +264,8 @@ class Oracle:
             outK = np.zeros((out_rows, R), dtype=np.uint8)
         if outV is None and not self.geom.latent_only:
             outV = np.zeros((out_rows, R), dtype=np.uint8)
-        err = self._L.ora_gather(
-            ctypes.byref(self._d), _ptr(M), int(layer), _ptr(bt), n_seqs, max_pages,
-            _ptr(st), _ptr(ln), _ptr(cu), _ptr(outK), _ptr(outV), out_rows,
-        )
+        err = fn(ctypes.byref(self._d), _ptr(M), int(layer), _ptr(bt), n_seqs, max_pages,
+                 _ptr(st), _ptr(ln), _ptr(cu), _ptr(outK), _ptr(outV), out_rows)
         return outK, outV, err
 
     # move ----------------------------------------------------------------
@@ -273,8 +286,9 @@ class Oracle:
                                      _ptr(v), 0 if v is None else v.size, _ptr(kd), _ptr(vd))
         return kd, vd, err
 
-    def gather_rows(self, layer, block_table, seq_len, cu, seq_start=None, out_rows=None):
-        """Byte offsets each output row reads: (ksrc[out_rows], vsrc[out_rows], err), -1 = untouched."""
+    def gather_rows(self, layer, block_table, seq_len, cu, seq_start=None, out_rows=None, kernel_facing=False):
+        """Byte offsets each output row reads: (ksrc[out_rows], vsrc[out_rows], err), -1 = untouched.
+        kernel_facing=True reads the table as gather_kf does."""
         bt = np.ascontiguousarray(block_table, dtype=np.int32)
         n_seqs, max_pages = bt.shape
         ln = np.ascontiguousarray(seq_len, dtype=np.int32)
@@ -284,8 +298,9 @@ class Oracle:
             out_rows = int(cu[-1]) if n_seqs > 0 else 0
         ks = np.full(out_rows, -1, np.int64)
         vs = np.full(out_rows, -1, np.int64)
-        err = self._L.ora_gather_rows(ctypes.byref(self._d), int(layer), _ptr(bt), n_seqs, max_pages,
-                                      _ptr(st), _ptr(ln), _ptr(cu), out_rows, _ptr(ks), _ptr(vs))
+        fn = self._L.ora_gather_kf_rows if kernel_facing else self._L.ora_gather_rows
+        err = fn(ctypes.byref(self._d), int(layer), _ptr(bt), n_seqs, max_pages,
+                 _ptr(st), _ptr(ln), _ptr(cu), out_rows, _ptr(ks), _ptr(vs))
         return ks, vs, err
 
     def move_rows(self, src_ids, dst_ids):

@@ -312,6 +312,8 @@ int ora_store_all(const ora_desc* d, uint8_t* M, const int64_t* slots, int64_t n
 
 /* ----------------------------------------------------------------- gather */
 
+static int decode_id(const ora_desc* d, int64_t id, int64_t* p, int64_t* o);
+
 /* Block-table read of one layer into packed [sum, H, D] K and V outputs: the
  * read the backends do through "one contiguous tensor + one shared block
  * table" (功能与动机). The report gives no gather call, so the plainest one
@@ -327,7 +329,7 @@ int ora_store_all(const ora_desc* d, uint8_t* M, const int64_t* slots, int64_t n
  * A page >= P raises ORA_E_ROW and the token is skipped. Skipped tokens leave
  * their output rows untouched. */
 static int gather_pass(const ora_desc* d, const uint8_t* M, int32_t layer,
-                       const int32_t* bt, int32_t n_seqs, int32_t max_pages,
+                       const int32_t* bt, int kernel_facing, int32_t n_seqs, int32_t max_pages,
                        const int32_t* seq_start, const int32_t* seq_len,
                        const int64_t* cu, uint8_t* outK, uint8_t* outV, int64_t out_rows,
                        int64_t* ksrc, int64_t* vsrc) {
@@ -351,6 +353,13 @@ static int gather_pass(const ora_desc* d, const uint8_t* M, int32_t layer,
             int64_t p = bt[(int64_t)s * max_pages + k];
             int64_t o = j % ps;
             if (p < 0) { p = 0; o = 0; }
+            else if (kernel_facing) {
+                /* the entry is a kernel-facing page (ora_block_table_kf): the
+                 * token's kernel-facing id is entry * ps + offset, decoded
+                 * back into (page, offset) as a move decodes its ids */
+                int e = decode_id(d, p * ps + o, &p, &o);
+                if (e != 0) { err |= e; continue; }
+            }
             if (p >= d->num_pages) { err |= ORA_E_ROW; continue; }
             int64_t r = cu[s] + (j - st);
             if (r < 0 || r >= out_rows) continue;
@@ -373,7 +382,7 @@ int ora_gather(const ora_desc* d, const uint8_t* M, int32_t layer,
                const int32_t* seq_start, const int32_t* seq_len,
                const int64_t* cu, uint8_t* outK, uint8_t* outV, int64_t out_rows) {
     if (M == NULL) return -1;
-    return gather_pass(d, M, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu,
+    return gather_pass(d, M, layer, bt, 0, n_seqs, max_pages, seq_start, seq_len, cu,
                        outK, outV, out_rows, NULL, NULL);
 }
 
@@ -382,7 +391,37 @@ int ora_gather(const ora_desc* d, const uint8_t* M, int32_t layer,
 int ora_gather_rows(const ora_desc* d, int32_t layer, const int32_t* bt, int32_t n_seqs,
                     int32_t max_pages, const int32_t* seq_start, const int32_t* seq_len,
                     const int64_t* cu, int64_t out_rows, int64_t* ksrc, int64_t* vsrc) {
-    return gather_pass(d, NULL, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu,
+    return gather_pass(d, NULL, layer, bt, 0, n_seqs, max_pages, seq_start, seq_len, cu,
+                       NULL, NULL, out_rows, ksrc, vsrc);
+}
+
+/* Gather through a kernel-facing block table, the read side of the report's
+ * prefix-only kernel-facing page table (关联脉络, PR #35247; the table is
+ * ora_block_table_kf's output). Reading taken: an entry e names the page
+ * whose token at offset o has the kernel-facing id e * ps + o, the id
+ * translate_kv_loc_for_kernel gives that token (关键源码片段
+ * multi_ended_allocator.py), so the gather decodes that id into (page,
+ * offset) exactly as a move decodes its ids and then reads as ora_gather.
+ * Consequences: a tombstoned virtual page, which the table build turns into
+ * entry 0, reads page 0 (the sink page) at the token's own offset; an entry
+ * that is not a multiple of the row-blocks per page raises ORA_E_FORM and
+ * an entry at or past P * 2L raises ORA_E_ROW (the token is skipped); a
+ * negative entry, which the table build never writes, reads the sink row
+ * (page 0, offset 0) as in ora_gather. Metadata checks are ora_gather's. */
+int ora_gather_kf(const ora_desc* d, const uint8_t* M, int32_t layer,
+                  const int32_t* kf_bt, int32_t n_seqs, int32_t max_pages,
+                  const int32_t* seq_start, const int32_t* seq_len,
+                  const int64_t* cu, uint8_t* outK, uint8_t* outV, int64_t out_rows) {
+    if (M == NULL) return -1;
+    return gather_pass(d, M, layer, kf_bt, 1, n_seqs, max_pages, seq_start, seq_len, cu,
+                       outK, outV, out_rows, NULL, NULL);
+}
+
+/* Address mode of ora_gather_kf (see ora_gather_rows). */
+int ora_gather_kf_rows(const ora_desc* d, int32_t layer, const int32_t* kf_bt, int32_t n_seqs,
+                       int32_t max_pages, const int32_t* seq_start, const int32_t* seq_len,
+                       const int64_t* cu, int64_t out_rows, int64_t* ksrc, int64_t* vsrc) {
+    return gather_pass(d, NULL, layer, kf_bt, 1, n_seqs, max_pages, seq_start, seq_len, cu,
                        NULL, NULL, out_rows, ksrc, vsrc);
 }
 

@@ -382,6 +382,64 @@ def pin_block_table_kf(so):
     assert err == oracle.E_TABLE
 
 
+def pin_gather_kf(so):
+    """Gather through a prefix-only kernel-facing block table
+    (tests/golden/gather_kf_tiny.txt, hand-computed): the table build gives
+    the listed entries, and every output row holds the K and V rows of the
+    listed (page, offset), read from the [P, 2L, ps, H, D] reference. Then:
+    on tables without tombstones the result equals the physical-page gather
+    of entry / 2L; an entry off the 2L grid raises E_FORM and one past the
+    pool E_ROW (rows untouched); a negative entry reads the sink row."""
+    L, H, D, it, ps, P = 2, 2, 8, 2, 4, 64
+    o = _mk(so, _geom(L, H, D, it, ps, P))
+    R = o.sizes()["row_bytes"]
+    v2p = np.arange(41, dtype=np.int32) + 10
+    v2p[7] = -1
+    rows = _rows(os.path.join(GOLDEN, "gather_kf_tiny.txt"))
+    trows = [r for r in rows if r[0] == "T"]
+    st = np.array([int(r[2]) for r in trows], np.int32)
+    ln = np.array([int(r[3]) for r in trows], np.int32)
+    virt = np.array([[int(x) for x in r[5:8]] for r in trows], np.int32)
+    want_kf = np.array([[int(x) for x in r[9:12]] for r in trows], np.int32)
+    kf, err = o.block_table_kf(virt, ln, v2p)
+    assert err == 0 and np.array_equal(kf, want_kf), kf
+    M = _fresh(o, seed=23)
+    env = strided_ref.envelope(M, L, H, D, it, ps, P)
+    g = synth.GatherBatch(kf, st, ln)
+    k, v, err = o.gather_kf(M, 1, kf, ln, g.cu, st)
+    rrows = [tuple(map(int, r[1:4])) for r in rows if r[0] == "R"]
+    assert err == 0 and k.shape[0] == len(rrows) == g.total
+    for r, page, off in rrows:
+        assert np.array_equal(k[r], env[page, 2, off].reshape(-1).view(np.uint8)), (r, page, off)
+        assert np.array_equal(v[r], env[page, 3, off].reshape(-1).view(np.uint8)), (r, page, off)
+    ks, vs, err = o.gather_rows(1, kf, ln, g.cu, st, kernel_facing=True)
+    assert err == 0
+    for r, page, off in rrows:
+        assert ks[r] == o.slot_row_byte(page * ps + off, 2) and vs[r] == o.slot_row_byte(page * ps + off, 3)
+    # without tombstones, the same rows as the physical gather of entry / 2L
+    rng = np.random.default_rng(21)
+    phys = rng.integers(1, P, size=(4, 5)).astype(np.int32)
+    gb = synth.GatherBatch(phys, np.array([0, 3, 7, 1], np.int32), np.array([20, 17, 9, 2], np.int32))
+    for layer in range(L):
+        k1, v1, e1 = o.gather_kf(M, layer, phys * (2 * L), gb.seq_len, gb.cu, gb.seq_start)
+        k2, v2, e2 = o.gather(M, layer, phys, gb.seq_len, gb.cu, gb.seq_start)
+        assert e1 == e2 == 0 and np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    # errors: off the grid (E_FORM), past the pool (E_ROW); those rows stay as they were
+    for entry, bit in ((5 * 2 * L + 1, oracle.E_FORM), (P * 2 * L, oracle.E_ROW)):
+        bt = np.array([[3 * 2 * L, entry]], np.int32)
+        gk = synth.GatherBatch(bt, np.zeros(1, np.int32), np.array([2 * ps], np.int32))
+        k, v, err = o.gather_kf(M, 0, bt, gk.seq_len, gk.cu, gk.seq_start)
+        assert err == bit, (entry, err)
+        assert np.array_equal(k[0], env[3, 0, 0].reshape(-1).view(np.uint8))
+        assert not k[ps:].any() and not v[ps:].any()
+    # a negative entry reads the sink row (page 0, offset 0) for every token
+    bt = np.array([[-1]], np.int32)
+    k, v, err = o.gather_kf(M, 1, bt, np.array([ps], np.int32), np.array([0, ps], np.int64))
+    assert err == 0 and all(np.array_equal(k[i], env[0, 2, 0].reshape(-1).view(np.uint8)) for i in range(ps))
+    assert all(np.array_equal(v[i], env[0, 3, 0].reshape(-1).view(np.uint8)) for i in range(ps))
+    assert R == 32
+
+
 def pin_mla(so):
     """MLA pools (one latent row per layer, blocks_per_page = L): hand-computed
     layout and ids (tests/golden/mla_tiny.txt), the id bound, the uniform-row
@@ -553,7 +611,7 @@ def pin_multiplier_one_collapse(so):
 PINS = [
     pin_translate_golden, pin_layout_table, pin_gates, pin_bijection, pin_store_vs_strided,
     pin_v2p_store, pin_gather_vs_strided, pin_roundtrip, pin_tail_untouched, pin_errors, pin_address_mode,
-    pin_block_table_kf, pin_mla, pin_mla_address_mode, pin_swa_token_map, pin_multiplier_one_collapse,
+    pin_block_table_kf, pin_gather_kf, pin_mla, pin_mla_address_mode, pin_swa_token_map, pin_multiplier_one_collapse,
 ]
 
 

@@ -87,6 +87,12 @@ MUTANTS = [
     ("block_table_prefix_floor",
      "int64_t np = len > 0 ? (len + ps - 1) / ps : 0;",
      "int64_t np = len > 0 ? len / ps : 0;"),
+    ("kf_gather_entry_read_as_physical_page",
+     "int e = decode_id(d, p * ps + o, &p, &o);",
+     "int e = decode_id(d, p * ps * blocks_of(d) + o, &p, &o);"),
+    ("kf_gather_drops_offset",
+     "int e = decode_id(d, p * ps + o, &p, &o);",
+     "int e = decode_id(d, p * ps, &p, &o);"),
     ("swa_map_skipped",
      "            else mapped = tmap[t];",
      "            else mapped = t;"),
