@@ -211,217 +211,6 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
   }
 }
 
-// ---------------------------------------------------------------------------
-// Bulk-copy form of the same gather (cp.async.bulk, the Hopper/Blackwell
-// bulk-copy engine): every warp runs one single-thread pipeline that stages
-// each chunk global -> shared (K and V, completion counted on an mbarrier)
-// and writes it back shared -> global with bulk stores, keeping up to
-// GTKV_BULK_STAGES - 1 chunks in flight. Items, clipping and error bits are
-// those of k_gather_runs. Used when a chunk fits its stage (R <= 4 KiB).
-#ifndef GTKV_GATHER_BULK
-#define GTKV_GATHER_BULK 0
-#endif
-#ifndef GTKV_BULK_WARPS
-#define GTKV_BULK_WARPS 4
-#endif
-#ifndef GTKV_BULK_STAGES
-#define GTKV_BULK_STAGES 4
-#endif
-constexpr int kBulkHalf = GTKV_GATHER_CHUNK;          // bytes of K (or V) a stage holds
-constexpr int kBulkStage = 2 * kBulkHalf;             // K then V
-constexpr unsigned kBulkSpinLimit = 1u << 24;         // mbarrier polls before giving up (~1 s)
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for a stage's loads: non-blocking polls with a short sleep,
-// at most kBulkSpinLimit of them (about a second); false = gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (unsigned spins = 0; spins < kBulkSpinLimit; ++spins) {
-    if (mbar_test_wait(bar, parity)) return true;
-    __nanosleep(32);
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-          "r"(smem_addr(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes, uint64_t pol) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
-               "r"(smem_addr(ssrc)), "r"(bytes), "l"(pol)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-template <bool PLANNED>
-__global__ void __launch_bounds__(32 * GTKV_BULK_WARPS) k_gather_bulk(
-    DevPool p, int32_t layer, const int32_t* __restrict__ bt, int32_t n_seqs, int32_t max_pages,
-    const int32_t* __restrict__ seq_start, const int32_t* __restrict__ seq_len, const int64_t* __restrict__ cu,
-    uint4* __restrict__ out_k, uint4* __restrict__ out_v, int64_t out_rows, int32_t chunk_rows,
-    int32_t chunks_per_page, const int32_t* __restrict__ plan, int batch) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int D = GTKV_BULK_STAGES;
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t ps = p.ps;
-  check_gather_meta(p, n_seqs, max_pages, seq_start, seq_len, cu, out_rows, tid, nthreads);
-  const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
-  int64_t n_units = n_entries;  // entries (table order) or plan positions, as in k_gather_runs
-  const int32_t* order = nullptr;
-  if constexpr (PLANNED) {
-    if (__ldg(plan + 1) != n_seqs || __ldg(plan + 2) != max_pages) {
-      if (tid == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
-      return;
-    }
-    if (__ldg(plan + 3) != 0) {
-      const int64_t np = __ldg(plan);
-      n_units = np < 0 ? 0 : (np > n_entries ? n_entries : np);
-      order = plan + 4 + p.num_pages + 1;
-    }
-  }
-
-  const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  uint8_t* buf = smem + static_cast<size_t>(wib) * D * kBulkStage;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(GTKV_BULK_WARPS) * D * kBulkStage) + wib * D;
-  if (lane == 0) {
-    for (int i = 0; i < D; ++i) mbar_init(bar + i);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  __syncwarp();
-
-  const int64_t vpr = p.vpr;
-  const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * ps;
-  const bool has_v = p.kv_rows == 2;
-  const int64_t n_items = n_units * chunks_per_page;
-  const int64_t it_step = nthreads >> 5;
-  const L2Policy pol = make_l2_policy();
-
-  // Pipeline state, uniform across the warp; lane 0 issues every bulk copy.
-  int64_t q_src[D];  // per stage: source (vector index from p.base), destination row, bytes
-  int64_t q_row[D];
-  uint32_t q_bytes[D];
-  int head = 0, tail = 0;  // items loaded / items stored
-  bool failed = false;
-
-  auto issue = [&](int st, int64_t src, int64_t row, uint32_t bytes) {
-    q_src[st] = src;
-    q_row[st] = row;
-    q_bytes[st] = bytes;
-    if (lane == 0) {
-      uint8_t* sb = buf + st * kBulkStage;
-      mbar_expect_tx(bar + st, has_v ? 2 * bytes : bytes);
-      bulk_load(sb, p.base + src, bytes, bar + st, pol.keep);
-      if (has_v) bulk_load(sb + kBulkHalf, p.base + src + ps * vpr, bytes, bar + st, pol.keep);
-    }
-  };
-  // Store the oldest loaded item; false when its load never landed.
-  auto retire = [&]() -> bool {
-    const int st = tail % D;
-    bool ok = true;
-    if (lane == 0) {
-      ok = mbar_wait_bounded(bar + st, (tail / D) & 1);
-      if (ok) {
-        uint8_t* sb = buf + st * kBulkStage;
-        bulk_store(out_k + q_row[st] * vpr, sb, q_bytes[st], pol.first);
-        if (has_v) bulk_store(out_v + q_row[st] * vpr, sb + kBulkHalf, q_bytes[st], pol.first);
-        bulk_commit();
-      }
-    }
-    ok = __shfl_sync(kFull, ok, 0);
-    ++tail;
-    return ok;
-  };
-
-  for (int64_t it0 = (tid >> 5) * batch; it0 < n_items && !failed; it0 += it_step * batch) {
-    // lane k < batch works out item it0 + k: empty, an error, a sink run, or a bulk run
-    const int64_t it = it0 + lane;
-    int64_t src = -1, row = 0;
-    uint32_t bytes = 0;
-    bool sink = false;
-    if (lane < batch && it < n_items) {
-      const int64_t u = it / chunks_per_page;
-      int64_t sk = u;
-      bool ok = true;
-      if (PLANNED && order != nullptr) {
-        sk = __ldg(order + u);
-        if (sk < 0 || sk >= n_entries) {
-          atomicOr(p.err, KV_DEV_ERR_TABLE);
-          ok = false;
-        }
-      }
-      Run r{0, 0, 0, 0};
-      if (ok)
-        r = gather_item(p, sk, it - u * chunks_per_page, koff, bt, max_pages, seq_start, seq_len, cu, out_rows,
-                        chunk_rows, true);
-      if (r.kind != 0) {
-        src = r.src;
-        row = r.row;
-        bytes = static_cast<uint32_t>(r.nvec * 16);
-        sink = r.kind == 2;
-      }
-    }
-    unsigned todo = __ballot_sync(kFull, src >= 0);
-    while (todo) {
-      const int k = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const long long isrc = __shfl_sync(kFull, src, k);
-      const long long irow = __shfl_sync(kFull, row, k);
-      const uint32_t ibytes = __shfl_sync(kFull, bytes, k);
-      if (__shfl_sync(kFull, sink, k)) {  // tombstoned entry: rows read the sink, copied by the warp
-        const int64_t nvec = ibytes / 16;
-        for (int64_t v = lane; v < nvec; v += 32) {
-          out_k[irow * vpr + v] = ld16<kLdNc>(p.base + isrc + v % vpr, pol);
-          if (has_v) out_v[irow * vpr + v] = ld16<kLdNc>(p.base + isrc + ps * vpr + v % vpr, pol);
-        }
-        continue;
-      }
-      if (head - tail == D) {  // every stage busy: retire the oldest, then reuse its stage
-        if (!retire()) {
-          failed = true;
-          break;
-        }
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-      }
-      issue(head % D, isrc, irow, ibytes);
-      ++head;
-    }
-  }
-  while (!failed && tail < head) {
-    if (!retire()) failed = true;
-  }
-  if (failed && lane == 0) {  // a load never landed: report, wait (bounded) for the others, drain
-    atomicOr(p.err, KV_DEV_ERR_TIMEOUT);
-    for (int u = tail; u < head; ++u) mbar_wait_bounded(bar + u % D, (u / D) & 1);
-  }
-  if (lane == 0) bulk_wait_all();
-}
-
 }  // namespace
 
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
@@ -439,33 +228,6 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
   };
   int64_t chunk_rows = rows_per_item(GTKV_GATHER_CHUNK);
   int64_t cpp = (p.ps + chunk_rows - 1) / chunk_rows;
-  if (GTKV_GATHER_BULK && chunk_rows * 16 * p.vpr <= kBulkHalf) {
-    constexpr int threads = 32 * GTKV_BULK_WARPS;
-    constexpr size_t smem = static_cast<size_t>(GTKV_BULK_WARPS) * GTKV_BULK_STAGES * (kBulkStage + 8);
-    auto bulk = plan ? k_gather_bulk<true> : k_gather_bulk<false>;
-    static bool attr[2] = {false, false};
-    if (!attr[plan ? 1 : 0]) {
-      cudaError_t e = cudaFuncSetAttribute(bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-      attr[plan ? 1 : 0] = true;
-    }
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, bulk, threads, smem) != cudaSuccess || nb < 1) nb = 1;
-    const int64_t n_items = static_cast<int64_t>(n_seqs) * max_pages * cpp;
-    int64_t blocks = (n_items + GTKV_BULK_WARPS - 1) / GTKV_BULK_WARPS;
-    const int64_t cap = static_cast<int64_t>(sm_count) * nb;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    const int64_t grid_warps = blocks * GTKV_BULK_WARPS;
-    int64_t batch = (n_items + grid_warps - 1) / grid_warps;
-    if (batch > GTKV_GATHER_MAX_BATCH) batch = GTKV_GATHER_MAX_BATCH;
-    if (batch < 1) batch = 1;
-    bulk<<<static_cast<unsigned>(blocks), threads, smem, s>>>(
-        p, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu, static_cast<uint4*>(out_k),
-        static_cast<uint4*>(out_v), out_rows, static_cast<int32_t>(chunk_rows), static_cast<int32_t>(cpp), plan,
-        static_cast<int>(batch));
-    return cudaGetLastError();
-  }
   // one round: 32 lanes x 8 vectors = 4 KiB of K and 4 KiB of V (latent: 8 KiB of K) in flight per warp
   auto kernel = latent ? (plan ? k_gather_runs<16, true, false> : k_gather_runs<16, false, false>)
                        : (plan ? k_gather_runs<8, true, true> : k_gather_runs<8, false, true>);

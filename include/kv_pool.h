@@ -80,7 +80,6 @@ enum {
 #define KV_DEV_ERR_TABLE 4 /* gather: sequence metadata inconsistent (see kv_gather_layer);
                               plan: the table changed while the plan was built */
 #define KV_DEV_ERR_FORM 8  /* move: an id was not p * ps * 2L + o with o < ps; pair skipped */
-#define KV_DEV_ERR_TIMEOUT 16 /* an asynchronous copy did not complete in time; the kernel stopped */
 
 typedef struct kv_pool kv_pool_t; /* opaque, host-side, owned by the library */
 

@@ -100,21 +100,6 @@ def test_entry_points_reject_null_pool(lib):
     assert lib.kv_pool_destroy(None) == 0
 
 
-def test_bulk_copy_gather_variant_compiles(tmp_path):
-    """The cp.async.bulk form of the gather (a compile-time alternative to the
-    vector-copy kernel) stays buildable for sm_103a."""
-    import subprocess
-
-    from gather_translate_kv_gb300 import build
-
-    src = build.os.path.join(build.CSRC, "kv_gather.cu")
-    out = tmp_path / "g.o"
-    cmd = [build.nvcc(), "-c", src, "-o", str(out)] + build.NVCC_FLAGS + \
-        ["-DGTKV_GATHER_BULK=1", "-DGTKV_BULK_WARPS=8", "-DGTKV_BULK_STAGES=2"]
-    subprocess.check_call(cmd)
-    assert out.exists()
-
-
 def c_abi_program(tmp_path, with_cuda: bool):
     """Build tests/c_abi_roundtrip.c as a plain C99 program against libgtkv.so."""
     import os
