@@ -119,6 +119,9 @@ def lib():
         "kv_gather_plan_noalloc": [vp, vp, i32, i32, vp, vp, vp, i64, vp],
         "kv_gather_layer_planned": [vp, i32, vp, i64, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
         "kv_translate_block_table": [vp, vp, i32, i32, vp, vp, i64, vp, vp],
+        "kv_gather_layer_kf": [vp, i32, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
+        "kv_gather_plan_kf": [vp, vp, i32, i32, vp, vp, vp, i64, vp],
+        "kv_gather_layer_planned_kf": [vp, i32, vp, i64, vp, i32, i32, vp, vp, vp, vp, vp, i64, vp],
         "kv_pool_last_error": [vp, vp, P(i32)],
     }
     for name, args in sig.items():
@@ -279,9 +282,8 @@ def kv_store_all_layers_slots(pool: KVPool, slots: torch.Tensor, k_all: torch.Te
         _stream(stream)))
 
 
-def kv_gather_layer(pool: KVPool, layer: int, block_table: torch.Tensor, seq_len: torch.Tensor,
-                    cu_out: torch.Tensor, out_k: torch.Tensor, out_v: torch.Tensor | None,
-                    seq_start: torch.Tensor | None = None, stream=None) -> None:
+def _gather(fn: str, pool: KVPool, layer: int, block_table: torch.Tensor, seq_len: torch.Tensor,
+            cu_out: torch.Tensor, out_k: torch.Tensor, out_v: torch.Tensor | None, seq_start, stream) -> None:
     if block_table.dim() != 2:
         raise ValueError("block_table must be [n_seqs, max_pages]")
     n_seqs, max_pages = block_table.shape
@@ -293,11 +295,24 @@ def kv_gather_layer(pool: KVPool, layer: int, block_table: torch.Tensor, seq_len
     ob = out_k.numel() * out_k.element_size()
     if ob % R != 0 or (out_v is not None and out_v.numel() * out_v.element_size() != ob):
         raise ValueError("out_k and out_v must be the same size, a whole number of rows")
-    _check("kv_gather_layer", lib().kv_gather_layer(
+    _check(fn, getattr(lib(), fn)(
         pool.handle, layer, _dev(block_table, "block_table", torch.int32), n_seqs, max_pages,
         _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
         _dev(cu_out, "cu_out", torch.int64), _dev(out_k, "out_k"), _dev(out_v, "out_v"), ob // R,
         _stream(stream)))
+
+
+def kv_gather_layer(pool: KVPool, layer: int, block_table: torch.Tensor, seq_len: torch.Tensor,
+                    cu_out: torch.Tensor, out_k: torch.Tensor, out_v: torch.Tensor | None,
+                    seq_start: torch.Tensor | None = None, stream=None) -> None:
+    _gather("kv_gather_layer", pool, layer, block_table, seq_len, cu_out, out_k, out_v, seq_start, stream)
+
+
+def kv_gather_layer_kf(pool: KVPool, layer: int, kf_table: torch.Tensor, seq_len: torch.Tensor,
+                       cu_out: torch.Tensor, out_k: torch.Tensor, out_v: torch.Tensor | None,
+                       seq_start: torch.Tensor | None = None, stream=None) -> None:
+    """kv_gather_layer through a kernel-facing table (kv_translate_block_table's output)."""
+    _gather("kv_gather_layer_kf", pool, layer, kf_table, seq_len, cu_out, out_k, out_v, seq_start, stream)
 
 
 def kv_gather_plan_bytes(pool: KVPool, n_seqs: int, max_pages: int) -> int:
@@ -306,20 +321,31 @@ def kv_gather_plan_bytes(pool: KVPool, n_seqs: int, max_pages: int) -> int:
     return out.value
 
 
+def _plan(fn: str, pool: KVPool, block_table, seq_len, seq_start, plan, stream) -> torch.Tensor:
+    n_seqs, max_pages = block_table.shape
+    nbytes = kv_gather_plan_bytes(pool, n_seqs, max_pages)
+    if plan is None:
+        plan = torch.empty(nbytes // 4, dtype=torch.int32, device=block_table.device)
+    _check(fn, getattr(lib(), fn)(
+        pool.handle, _dev(block_table, "block_table", torch.int32), n_seqs, max_pages,
+        _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
+        _dev(plan, "plan", torch.int32), plan.numel() * 4, _stream(stream)))
+    return plan
+
+
 def kv_gather_plan(pool: KVPool, block_table: torch.Tensor, seq_len: torch.Tensor,
                    seq_start: torch.Tensor | None = None, plan: torch.Tensor | None = None,
                    stream=None) -> torch.Tensor:
     """Page-major plan of a block table (an int32 device tensor, allocated
     here when not given); reuse it for every layer's gather of the step."""
-    n_seqs, max_pages = block_table.shape
-    nbytes = kv_gather_plan_bytes(pool, n_seqs, max_pages)
-    if plan is None:
-        plan = torch.empty(nbytes // 4, dtype=torch.int32, device=block_table.device)
-    _check("kv_gather_plan", lib().kv_gather_plan(
-        pool.handle, _dev(block_table, "block_table", torch.int32), n_seqs, max_pages,
-        _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
-        _dev(plan, "plan", torch.int32), plan.numel() * 4, _stream(stream)))
-    return plan
+    return _plan("kv_gather_plan", pool, block_table, seq_len, seq_start, plan, stream)
+
+
+def kv_gather_plan_kf(pool: KVPool, kf_table: torch.Tensor, seq_len: torch.Tensor,
+                      seq_start: torch.Tensor | None = None, plan: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """kv_gather_plan over a kernel-facing table (entries phys * 2L)."""
+    return _plan("kv_gather_plan_kf", pool, kf_table, seq_len, seq_start, plan, stream)
 
 
 def kv_gather_plan_noalloc(pool: KVPool, block_table: torch.Tensor, seq_len: torch.Tensor, plan: torch.Tensor,
@@ -338,19 +364,35 @@ def kv_gather_plan_noalloc(pool: KVPool, block_table: torch.Tensor, seq_len: tor
     return plan
 
 
-def kv_gather_layer_planned(pool: KVPool, layer: int, plan: torch.Tensor, block_table: torch.Tensor,
-                            seq_len: torch.Tensor, cu_out: torch.Tensor, out_k: torch.Tensor,
-                            out_v: torch.Tensor | None, seq_start: torch.Tensor | None = None, stream=None) -> None:
+def _gather_planned(fn: str, pool: KVPool, layer: int, plan: torch.Tensor, block_table: torch.Tensor,
+                    seq_len: torch.Tensor, cu_out: torch.Tensor, out_k: torch.Tensor, out_v: torch.Tensor | None,
+                    seq_start, stream) -> None:
     n_seqs, max_pages = block_table.shape
     R = pool.row_bytes
     ob = out_k.numel() * out_k.element_size()
     if ob % R != 0 or (out_v is not None and out_v.numel() * out_v.element_size() != ob):
         raise ValueError("out_k and out_v must be the same size, a whole number of rows")
-    _check("kv_gather_layer_planned", lib().kv_gather_layer_planned(
+    _check(fn, getattr(lib(), fn)(
         pool.handle, layer, _dev(plan, "plan", torch.int32), plan.numel() * 4,
         _dev(block_table, "block_table", torch.int32),
         n_seqs, max_pages, _dev(seq_start, "seq_start", torch.int32), _dev(seq_len, "seq_len", torch.int32),
         _dev(cu_out, "cu_out", torch.int64), _dev(out_k, "out_k"), _dev(out_v, "out_v"), ob // R, _stream(stream)))
+
+
+def kv_gather_layer_planned(pool: KVPool, layer: int, plan: torch.Tensor, block_table: torch.Tensor,
+                            seq_len: torch.Tensor, cu_out: torch.Tensor, out_k: torch.Tensor,
+                            out_v: torch.Tensor | None, seq_start: torch.Tensor | None = None, stream=None) -> None:
+    _gather_planned("kv_gather_layer_planned", pool, layer, plan, block_table, seq_len, cu_out, out_k, out_v,
+                    seq_start, stream)
+
+
+def kv_gather_layer_planned_kf(pool: KVPool, layer: int, plan: torch.Tensor, kf_table: torch.Tensor,
+                               seq_len: torch.Tensor, cu_out: torch.Tensor, out_k: torch.Tensor,
+                               out_v: torch.Tensor | None, seq_start: torch.Tensor | None = None,
+                               stream=None) -> None:
+    """kv_gather_layer_planned over a kernel-facing table, with a kv_gather_plan_kf plan."""
+    _gather_planned("kv_gather_layer_planned_kf", pool, layer, plan, kf_table, seq_len, cu_out, out_k, out_v,
+                    seq_start, stream)
 
 
 def kv_move(pool: KVPool, src_ids: torch.Tensor, dst_ids: torch.Tensor, stream=None) -> None:

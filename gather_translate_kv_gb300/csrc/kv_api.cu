@@ -285,8 +285,9 @@ int kv_store_all_layers_slots(const kv_pool_t* pool, const int64_t* slots_dev, i
 }
 
 static int gather(const kv_pool_t* pool, int32_t layer, const void* plan_dev, const int32_t* block_table_dev,
-                  int32_t n_seqs, int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
-                  const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream) {
+                  bool kernel_facing, int32_t n_seqs, int32_t max_pages, const int32_t* seq_start_dev,
+                  const int32_t* seq_len_dev, const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev,
+                  int64_t out_rows, kv_stream_t stream) {
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   if (layer < 0 || layer >= pool->desc.layer_num || n_seqs < 0 || max_pages < 0 || out_rows < 0)
@@ -305,7 +306,8 @@ static int gather(const kv_pool_t* pool, int32_t layer, const void* plan_dev, co
     return KV_ERR_ALIGN;
   return launched(gtkv::launch_gather(pool->dev, layer, block_table_dev, n_seqs, max_pages, seq_start_dev,
                                       seq_len_dev, cu_out_dev, out_k_dev, out_v_dev, out_rows,
-                                      static_cast<const int32_t*>(plan_dev), pool->sm_count, as_stream(stream)));
+                                      static_cast<const int32_t*>(plan_dev), kernel_facing, pool->sm_count,
+                                      as_stream(stream)));
 }
 
 int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_table_dev, int32_t n_seqs,
@@ -313,8 +315,17 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
                     const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
                     kv_stream_t stream) {
   Range nvtx("kv_gather_layer");
-  return gather(pool, layer, nullptr, block_table_dev, n_seqs, max_pages, seq_start_dev, seq_len_dev, cu_out_dev,
-                out_k_dev, out_v_dev, out_rows, stream);
+  return gather(pool, layer, nullptr, block_table_dev, false, n_seqs, max_pages, seq_start_dev, seq_len_dev,
+                cu_out_dev, out_k_dev, out_v_dev, out_rows, stream);
+}
+
+int kv_gather_layer_kf(const kv_pool_t* pool, int32_t layer, const int32_t* kf_table_dev, int32_t n_seqs,
+                       int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
+                       const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
+                       kv_stream_t stream) {
+  Range nvtx("kv_gather_layer_kf");
+  return gather(pool, layer, nullptr, kf_table_dev, true, n_seqs, max_pages, seq_start_dev, seq_len_dev,
+                cu_out_dev, out_k_dev, out_v_dev, out_rows, stream);
 }
 
 int kv_gather_plan_bytes(const kv_pool_t* pool, int32_t n_seqs, int32_t max_pages, int64_t* plan_bytes) {
@@ -324,10 +335,9 @@ int kv_gather_plan_bytes(const kv_pool_t* pool, int32_t n_seqs, int32_t max_page
   return KV_OK;
 }
 
-int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
-                   const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,
-                   kv_stream_t stream) {
-  Range nvtx("kv_gather_plan");
+static int gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, bool kernel_facing, int32_t n_seqs,
+                       int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev,
+                       int64_t plan_bytes, kv_stream_t stream) {
   int rc = enter(pool);
   if (rc != KV_OK) return rc;
   int64_t need = 0;
@@ -339,8 +349,37 @@ int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_
       (reinterpret_cast<uintptr_t>(block_table_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_start_dev) & 3u))
     return KV_ERR_ALIGN;
   return launched(gtkv::launch_gather_plan(pool->dev, block_table_dev, n_seqs, max_pages, seq_start_dev,
-                                           seq_len_dev, static_cast<int32_t*>(plan_dev), pool->sm_count,
-                                           as_stream(stream)));
+                                           seq_len_dev, static_cast<int32_t*>(plan_dev), kernel_facing,
+                                           pool->sm_count, as_stream(stream)));
+}
+
+int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
+                   const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,
+                   kv_stream_t stream) {
+  Range nvtx("kv_gather_plan");
+  return gather_plan(pool, block_table_dev, false, n_seqs, max_pages, seq_start_dev, seq_len_dev, plan_dev,
+                     plan_bytes, stream);
+}
+
+int kv_gather_plan_kf(const kv_pool_t* pool, const int32_t* kf_table_dev, int32_t n_seqs, int32_t max_pages,
+                      const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,
+                      kv_stream_t stream) {
+  Range nvtx("kv_gather_plan_kf");
+  return gather_plan(pool, kf_table_dev, true, n_seqs, max_pages, seq_start_dev, seq_len_dev, plan_dev,
+                     plan_bytes, stream);
+}
+
+static int gather_planned(const kv_pool_t* pool, int32_t layer, const void* plan_dev, int64_t plan_bytes,
+                          const int32_t* block_table_dev, bool kernel_facing, int32_t n_seqs, int32_t max_pages,
+                          const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
+                          void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream) {
+  if (plan_dev == nullptr) return KV_ERR_INVALID;
+  int64_t need = 0;
+  const int rc = kv_gather_plan_bytes(pool, n_seqs, max_pages, &need);
+  if (rc != KV_OK) return rc;
+  if (plan_bytes < need) return KV_ERR_INVALID;  // the kernel reads up to `need` bytes of the plan
+  return gather(pool, layer, plan_dev, block_table_dev, kernel_facing, n_seqs, max_pages, seq_start_dev,
+                seq_len_dev, cu_out_dev, out_k_dev, out_v_dev, out_rows, stream);
 }
 
 int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* plan_dev, int64_t plan_bytes,
@@ -348,13 +387,17 @@ int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* pl
                             const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
                             void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream) {
   Range nvtx("kv_gather_layer_planned");
-  if (plan_dev == nullptr) return KV_ERR_INVALID;
-  int64_t need = 0;
-  const int rc = kv_gather_plan_bytes(pool, n_seqs, max_pages, &need);
-  if (rc != KV_OK) return rc;
-  if (plan_bytes < need) return KV_ERR_INVALID;  // the kernel reads up to `need` bytes of the plan
-  return gather(pool, layer, plan_dev, block_table_dev, n_seqs, max_pages, seq_start_dev, seq_len_dev, cu_out_dev,
-                out_k_dev, out_v_dev, out_rows, stream);
+  return gather_planned(pool, layer, plan_dev, plan_bytes, block_table_dev, false, n_seqs, max_pages, seq_start_dev,
+                        seq_len_dev, cu_out_dev, out_k_dev, out_v_dev, out_rows, stream);
+}
+
+int kv_gather_layer_planned_kf(const kv_pool_t* pool, int32_t layer, const void* plan_dev, int64_t plan_bytes,
+                               const int32_t* kf_table_dev, int32_t n_seqs, int32_t max_pages,
+                               const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
+                               void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream) {
+  Range nvtx("kv_gather_layer_planned_kf");
+  return gather_planned(pool, layer, plan_dev, plan_bytes, kf_table_dev, true, n_seqs, max_pages, seq_start_dev,
+                        seq_len_dev, cu_out_dev, out_k_dev, out_v_dev, out_rows, stream);
 }
 
 int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* dst_ids_dev, int64_t n,

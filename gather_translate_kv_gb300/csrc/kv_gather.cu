@@ -19,6 +19,7 @@
 // search and no host synchronization: the item space is n_seqs x max_pages x
 // chunks_per_page, and an entry outside a sequence's window is an empty item.
 #include "kv_launch.h"
+#include "kv_plan.cuh"
 
 namespace gtkv {
 
@@ -29,6 +30,19 @@ namespace {
 #endif
 #ifndef GTKV_GATHER_MAX_BATCH
 #define GTKV_GATHER_MAX_BATCH 8  // consecutive items a warp takes at once (1..32)
+#endif
+#ifndef GTKV_GATHER_CHV
+#define GTKV_GATHER_CHV 8  // 16-byte vectors of K (and as many of V) each lane keeps in flight
+#endif
+// Blocks per SM the register allocation must allow (0: left to the compiler,
+// which keeps these kernels at 2 blocks of 256 threads per SM).
+#ifndef GTKV_GATHER_MINB
+#define GTKV_GATHER_MINB 0
+#endif
+#if GTKV_GATHER_MINB > 0
+#define GTKV_GATHER_BOUNDS __launch_bounds__(kBlock, GTKV_GATHER_MINB)
+#else
+#define GTKV_GATHER_BOUNDS __launch_bounds__(kBlock)
 #endif
 
 // Metadata checks, one sequence per thread, grid-stride (they never gate the
@@ -52,6 +66,10 @@ __device__ __forceinline__ void check_gather_meta(const DevPool& p, int32_t n_se
 
 // One work item: chunk c of block-table entry sk = s*max_pages + k, clipped to
 // the window [start_s, len_s), to tokens >= 0 and to output rows [0, out_rows).
+// With KF the table holds kernel-facing entries phys * 2L (2L = the
+// row-blocks per page, L for MLA: the prefix-only table of
+// kv_translate_block_table): entry * ps + o is then the token's kernel-facing
+// id, so the page is entry / 2L and an entry off that grid is a form error.
 struct Run {
   int64_t src;   // 16-byte vector index (from p.base) of its first K row; V is ps rows later
   int64_t row;   // first output row
@@ -59,6 +77,7 @@ struct Run {
   int kind;      // 0: nothing to copy; 1: rows of a page; 2: tombstoned entry, every row reads the sink
 };
 
+template <bool KF>
 __device__ __forceinline__ Run gather_item(const DevPool& p, int64_t sk, int64_t c, int64_t koff,
                                            const int32_t* __restrict__ bt, int32_t max_pages,
                                            const int32_t* __restrict__ seq_start,
@@ -77,10 +96,19 @@ __device__ __forceinline__ Run gather_item(const DevPool& p, int64_t sk, int64_t
   if (jhi > (k + 1) * ps) jhi = (k + 1) * ps;
   if (jhi > b) jhi = b;
   if (jlo >= jhi) return r;  // entry outside the window: empty item
-  const int64_t page = __ldg(bt + sk);
-  if (page >= p.num_pages) {
+  int64_t page = __ldg(bt + sk);
+  if (page >= p.num_pages * (KF ? p.blocks : 1)) {  // a page (or kernel-facing entry) past the pool
     if (report) atomicOr(p.err, KV_DEV_ERR_ROW);
     return r;
+  }
+  if (KF && page > 0) {  // 0 < entry < P * 2L < 2^31: 32-bit arithmetic
+    const uint32_t e = static_cast<uint32_t>(page), b = static_cast<uint32_t>(p.blocks);
+    const uint32_t phys = e / b;
+    if (phys * b != e) {
+      if (report) atomicOr(p.err, KV_DEV_ERR_FORM);
+      return r;
+    }
+    page = phys;
   }
   const int64_t cs = __ldg(cu + s);
   int64_t rlo = cs + (jlo - a);
@@ -107,9 +135,10 @@ __device__ __forceinline__ Run gather_item(const DevPool& p, int64_t sk, int64_t
 // Items = (table entry sk, chunk c), taken in table order, or in the order of
 // a page-major plan (PLANNED: kv_plan.cu). CHV 16-byte vectors per lane per
 // round: one round moves 32*CHV vectors of K and, with HAS_V, as many of V
-// (a latent-only pool has no V rows).
-template <int CHV, bool PLANNED, bool HAS_V>
-__global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer, const int32_t* __restrict__ bt,
+// (a latent-only pool has no V rows). KF: the table holds kernel-facing
+// entries (see gather_item).
+template <int CHV, bool PLANNED, bool HAS_V, bool KF>
+__global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const int32_t* __restrict__ bt,
                                                         int32_t n_seqs, int32_t max_pages,
                                                         const int32_t* __restrict__ seq_start,
                                                         const int32_t* __restrict__ seq_len,
@@ -124,14 +153,16 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
   int64_t n_units = n_entries;  // entries (table order) or plan positions
   const int32_t* order = nullptr;
   if constexpr (PLANNED) {
-    // the plan must have been built for a table of this shape; its entries
-    // are bounds-checked one by one below, so a stale plan can only give
-    // wrong rows (flagged), never an access outside the buffers
-    if (__ldg(plan + 1) != n_seqs || __ldg(plan + 2) != max_pages) {
+    // the plan must have been built for a table of this shape and form; its
+    // entries are bounds-checked one by one below, so a stale plan can only
+    // give wrong rows (flagged), never an access outside the buffers
+    const int32_t flags = __ldg(plan + 3);
+    if (__ldg(plan + 1) != n_seqs || __ldg(plan + 2) != max_pages ||
+        ((flags & kPlanKernelFacing) != 0) != KF) {
       if (tid == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
       return;
     }
-    if (__ldg(plan + 3) != 0) {  // page-major order pays; else keep the table's order
+    if (flags & kPlanPageMajor) {  // page-major order pays; else keep the table's order
       const int64_t np = __ldg(plan);
       n_units = np < 0 ? 0 : (np > n_entries ? n_entries : np);
       order = plan + 4 + p.num_pages + 1;
@@ -168,7 +199,8 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
           ok = false;
         }
       }
-      if (ok) mine = gather_item(p, sk, c, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows, true);
+      if (ok)
+        mine = gather_item<KF>(p, sk, c, koff, bt, max_pages, seq_start, seq_len, cu, out_rows, chunk_rows, true);
     }
     const int nb = n_items - it0 < batch ? static_cast<int>(n_items - it0) : batch;
     for (int j = 0; j < nb; ++j) {
@@ -215,7 +247,8 @@ __global__ void __launch_bounds__(kBlock) k_gather_runs(DevPool p, int32_t layer
 
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
                           const int32_t* seq_start, const int32_t* seq_len, const int64_t* cu, void* out_k,
-                          void* out_v, int64_t out_rows, const int32_t* plan, int sm_count, cudaStream_t s) {
+                          void* out_v, int64_t out_rows, const int32_t* plan, bool kernel_facing, int sm_count,
+                          cudaStream_t s) {
   // rows per item: GTKV_GATHER_CHUNK bytes of K (and as many of V); a
   // latent-only pool has no V, so its items take twice the K bytes and keep
   // the same bytes in flight per warp
@@ -229,8 +262,14 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
   int64_t chunk_rows = rows_per_item(GTKV_GATHER_CHUNK);
   int64_t cpp = (p.ps + chunk_rows - 1) / chunk_rows;
   // one round: 32 lanes x 8 vectors = 4 KiB of K and 4 KiB of V (latent: 8 KiB of K) in flight per warp
-  auto kernel = latent ? (plan ? k_gather_runs<16, true, false> : k_gather_runs<16, false, false>)
-                       : (plan ? k_gather_runs<8, true, true> : k_gather_runs<8, false, true>);
+  constexpr int CHV = GTKV_GATHER_CHV;
+  using Kernel = decltype(&k_gather_runs<CHV, true, true, false>);
+  const Kernel kernels[2][2][2] = {  // [latent][plan][kernel_facing]
+      {{k_gather_runs<CHV, false, true, false>, k_gather_runs<CHV, false, true, true>},
+       {k_gather_runs<CHV, true, true, false>, k_gather_runs<CHV, true, true, true>}},
+      {{k_gather_runs<2 * CHV, false, false, false>, k_gather_runs<2 * CHV, false, false, true>},
+       {k_gather_runs<2 * CHV, true, false, false>, k_gather_runs<2 * CHV, true, false, true>}}};
+  const Kernel kernel = kernels[latent][plan != nullptr][kernel_facing];
   if (latent) {
     chunk_rows = rows_per_item(2 * GTKV_GATHER_CHUNK);
     cpp = (p.ps + chunk_rows - 1) / chunk_rows;

@@ -15,12 +15,14 @@ cudaError_t launch_store_slots(const DevPool& p, int32_t layer0, int32_t n_layer
                                cudaStream_t s);
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
                           const int32_t* seq_start, const int32_t* seq_len, const int64_t* cu, void* out_k,
-                          void* out_v, int64_t out_rows, const int32_t* plan, int sm_count, cudaStream_t s);
+                          void* out_v, int64_t out_rows, const int32_t* plan, bool kernel_facing, int sm_count,
+                          cudaStream_t s);
 // Page-major gather plan (kv_plan.cu): its size in int32 words, and its build.
+// kernel_facing: the table holds kernel-facing entries phys * 2L.
 int64_t plan_words(const DevPool& p, int32_t n_seqs, int32_t max_pages);
 cudaError_t launch_gather_plan(const DevPool& p, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
-                               const int32_t* seq_start, const int32_t* seq_len, int32_t* plan, int sm_count,
-                               cudaStream_t s);
+                               const int32_t* seq_start, const int32_t* seq_len, int32_t* plan, bool kernel_facing,
+                               int sm_count, cudaStream_t s);
 cudaError_t launch_translate_mapped(const DevPool& p, const int64_t* slots, int64_t n, const int64_t* tmap,
                                     int64_t tmap_len, const int32_t* v2p, int64_t v2p_len, int32_t* ids, int sm_count,
                                     cudaStream_t s);

@@ -12,9 +12,11 @@
 // The plan is a counting sort of the entries by page, in a caller-provided
 // buffer (int32 words):
 //   [0] number of entries in the plan   [1] n_seqs   [2] max_pages
-//   [3] 1 when the page-major order pays (entries >= 1.5 x distinct pages),
-//       0 when pages are hardly shared and the table's own order is better
-//       (the output writes stay sequential); the planned gather follows it
+//   [3] flags: bit 0 (kPlanPageMajor) when the page-major order pays
+//       (entries >= 1.5 x distinct pages), clear when pages are hardly shared
+//       and the table's own order is better (the output writes stay
+//       sequential), and the planned gather follows it; bit 1
+//       (kPlanKernelFacing) when the table holds kernel-facing entries
 //   [4 .. 4+P]            per-page counts, then start offsets (P + 1 words)
 //   [5+P .. 5+P+S*maxp)   entry indices s*max_pages + k, grouped by page
 // Only entries whose tokens overlap the sequence's window [start, len) enter
@@ -29,12 +31,13 @@ namespace {
 
 __global__ void __launch_bounds__(kBlock) k_plan_count(DevPool p, const int32_t* __restrict__ bt, int64_t n_entries,
                                                        int32_t max_pages, const int32_t* __restrict__ seq_start,
-                                                       const int32_t* __restrict__ seq_len, int32_t* __restrict__ plan) {
+                                                       const int32_t* __restrict__ seq_len, int32_t bt_div,
+                                                       int32_t* __restrict__ plan) {
   int32_t* counts = plan + kPlanHeaderWords;
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
-    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
+    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bt_div, bits);
     if (b >= 0) atomicAdd(counts + b, 1);
   }
   if (bits) atomicOr(p.err, bits);
@@ -42,25 +45,25 @@ __global__ void __launch_bounds__(kBlock) k_plan_count(DevPool p, const int32_t*
 
 // Counts -> start offsets (in place) and the plan header.
 __global__ void __launch_bounds__(kScanThreads) k_plan_scan(int64_t n_buckets, int32_t n_seqs, int32_t max_pages,
-                                                            int32_t* __restrict__ plan) {
-  scan_plan_counts(plan + kPlanHeaderWords, n_buckets, n_seqs, max_pages, plan);
+                                                            int32_t form_flag, int32_t* __restrict__ plan) {
+  scan_plan_counts(plan + kPlanHeaderWords, n_buckets, n_seqs, max_pages, form_flag, plan);
 }
 
 __global__ void __launch_bounds__(kBlock) k_plan_scatter(DevPool p, const int32_t* __restrict__ bt,
                                                          int64_t n_entries, int32_t max_pages,
                                                          const int32_t* __restrict__ seq_start,
-                                                         const int32_t* __restrict__ seq_len,
+                                                         const int32_t* __restrict__ seq_len, int32_t bt_div,
                                                          int32_t* __restrict__ plan) {
   int32_t* offs = plan + kPlanHeaderWords;
   int32_t* entries = offs + p.num_pages + 1;
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
-    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
+    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bt_div, bits);
     if (b >= 0) plan_place(entries, offs + b, n_entries, e, bits);
   }
-  // page >= P entries were already reported by the count pass; a position
-  // past the plan means the table changed under the build
+  // page >= P and off-grid entries were already reported by the count pass;
+  // a position past the plan means the table changed under the build
   if (bits & KV_DEV_ERR_TABLE) atomicOr(p.err, KV_DEV_ERR_TABLE);
 }
 
@@ -71,17 +74,19 @@ int64_t plan_words(const DevPool& p, int32_t n_seqs, int32_t max_pages) {
 }
 
 cudaError_t launch_gather_plan(const DevPool& p, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
-                               const int32_t* seq_start, const int32_t* seq_len, int32_t* plan, int sm_count,
-                               cudaStream_t s) {
+                               const int32_t* seq_start, const int32_t* seq_len, int32_t* plan, bool kernel_facing,
+                               int sm_count, cudaStream_t s) {
   const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
+  const int32_t bt_div = kernel_facing ? p.blocks : 1;
   cudaError_t e = cudaMemsetAsync(plan, 0, sizeof(int32_t) * (kPlanHeaderWords + p.num_pages + 1), s);
   if (e != cudaSuccess) return e;
   const unsigned grid = grid_for(k_plan_count, (n_entries + 31) / 32, sm_count);
-  k_plan_count<<<grid, kBlock, 0, s>>>(p, bt, n_entries, max_pages, seq_start, seq_len, plan);
+  k_plan_count<<<grid, kBlock, 0, s>>>(p, bt, n_entries, max_pages, seq_start, seq_len, bt_div, plan);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_plan_scan<<<1, kScanThreads, 0, s>>>(p.num_pages, n_seqs, max_pages, plan);
+  k_plan_scan<<<1, kScanThreads, 0, s>>>(p.num_pages, n_seqs, max_pages, kernel_facing ? kPlanKernelFacing : 0,
+                                         plan);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_plan_scatter<<<grid, kBlock, 0, s>>>(p, bt, n_entries, max_pages, seq_start, seq_len, plan);
+  k_plan_scatter<<<grid, kBlock, 0, s>>>(p, bt, n_entries, max_pages, seq_start, seq_len, bt_div, plan);
   return cudaGetLastError();
 }
 

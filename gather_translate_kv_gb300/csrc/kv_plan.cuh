@@ -7,27 +7,41 @@
 
 namespace gtkv {
 
-constexpr int kPlanHeaderWords = 4;  // entries, n_seqs, max_pages, page-major flag
+constexpr int kPlanHeaderWords = 4;  // entries, n_seqs, max_pages, flags
+// Bits of the plan's flags word [3].
+constexpr int32_t kPlanPageMajor = 1;      // the page-major order pays: walk the plan, not the table
+constexpr int32_t kPlanKernelFacing = 2;   // built from a table of kernel-facing entries (phys * 2L)
 
 // Page bucket of block-table entry e = s * max_pages + k, or -1 when the entry
 // holds no token of the sequence's window [start_s, len_s). A tombstone
 // (negative page) reads the page-0 sink and joins page 0; a page >= P sets
-// KV_DEV_ERR_ROW in `bits` and is left out.
+// KV_DEV_ERR_ROW in `bits` and is left out. bt_div > 1: the table holds
+// kernel-facing entries phys * bt_div (bt_div = the row-blocks per page);
+// one off that grid sets KV_DEV_ERR_FORM and is left out.
 __device__ __forceinline__ int64_t plan_bucket(const DevPool& p, int64_t e, const int32_t* __restrict__ bt,
                                                int32_t max_pages, const int32_t* __restrict__ seq_start,
-                                               const int32_t* __restrict__ seq_len, int& bits) {
+                                               const int32_t* __restrict__ seq_len, int32_t bt_div, int& bits) {
   const int64_t s = e / max_pages;
   const int64_t k = e - s * max_pages;
   int64_t lo = seq_start ? __ldg(seq_start + s) : 0;
   if (lo < 0) lo = 0;
   const int64_t hi = __ldg(seq_len + s);
   if (k * p.ps >= hi || (k + 1) * p.ps <= lo) return -1;
-  const int64_t page = __ldg(bt + e);
-  if (page >= p.num_pages) {
+  int64_t page = __ldg(bt + e);
+  if (page >= p.num_pages * bt_div) {
     bits |= KV_DEV_ERR_ROW;
     return -1;
   }
-  return page < 0 ? 0 : page;
+  if (page <= 0) return 0;
+  if (bt_div != 1) {
+    const int64_t phys = page / bt_div;
+    if (phys * bt_div != page) {
+      bits |= KV_DEV_ERR_FORM;
+      return -1;
+    }
+    page = phys;
+  }
+  return page;
 }
 
 // Scatter step of the counting sort: entry e takes the next position of its
@@ -54,10 +68,11 @@ constexpr int kScanAhead = 4;                            // tiles whose loads ar
 // threads: tile after tile of 4096 counters (thread t owns 4 consecutive
 // ones), kScanAhead tiles loaded before any is scanned, a running carry
 // between tiles. Then counts[n_pages] = total and the plan header: [0] total
-// entries, [1] n_seqs, [2] max_pages, [3] 1 when entries >= 1.5 x distinct
-// pages (the page-major order pays), else 0.
+// entries, [1] n_seqs, [2] max_pages, [3] flags: kPlanPageMajor when entries
+// >= 1.5 x distinct pages (the page-major order pays), plus `form_flag`
+// (kPlanKernelFacing or 0).
 __device__ __forceinline__ void scan_plan_counts(int32_t* counts, int64_t n_pages, int32_t n_seqs,
-                                                 int32_t max_pages, int32_t* __restrict__ plan) {
+                                                 int32_t max_pages, int32_t form_flag, int32_t* __restrict__ plan) {
   __shared__ int32_t warp_sum[kScanThreads / 32];
   __shared__ int32_t pages_used;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -117,7 +132,8 @@ __device__ __forceinline__ void scan_plan_counts(int32_t* counts, int64_t n_page
     plan[0] = carry;
     plan[1] = n_seqs;
     plan[2] = max_pages;
-    plan[3] = 2 * static_cast<int64_t>(carry) >= 3 * static_cast<int64_t>(pages_used) ? 1 : 0;
+    plan[3] = (2 * static_cast<int64_t>(carry) >= 3 * static_cast<int64_t>(pages_used) ? kPlanPageMajor : 0) |
+              form_flag;
   }
 }
 

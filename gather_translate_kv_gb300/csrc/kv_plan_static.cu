@@ -16,6 +16,7 @@
 // share it and it keeps the last call's contents, so each call clears the
 // counters it uses first, on its own stream. Calls that overlap on the GPU
 // (other streams, threads or pools on the same device) race on it.
+#include <cuda.h>  // CUcontext and the driver's function types only: the functions are looked up at run time
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
@@ -37,21 +38,59 @@ constexpr int kMaxDevices = 128;
 // stand-in for the array; kernels get its device address from counts_on().
 static __device__ __align__(256) int32_t g_plan_counts[kMaxPages + 1];
 
-int32_t* g_counts_addr[kMaxDevices] = {};
+// The array's address per device, with the id of the context it was looked
+// up in: a context the runtime creates anew (after cudaDeviceReset, for
+// instance) loads the module again, and the array may move.
+struct CountsAddr {
+  int32_t* ptr;
+  unsigned long long ctx_id;
+};
+CountsAddr g_counts_addr[kMaxDevices] = {};
 std::mutex g_counts_mu;
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Process-unique id of the calling thread's current context (the driver
+// never reuses one), or an error when the thread has none bound yet.
+// Called with g_counts_mu held.
+cudaError_t current_context_id(unsigned long long* id) {
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) {
+    void* f0 = nullptr;
+    void* f1 = nullptr;
+    cudaDriverEntryPointQueryResult q0, q1;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 12000, cudaEnableDefault, &q0) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q0 != cudaDriverEntryPointSuccess || q1 != cudaDriverEntryPointSuccess)
+      return cudaErrorNotSupported;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f0);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f1);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
 // Device address of g_plan_counts on `device`, which must be current. Looked
-// up on the first call per device and kept.
+// up with cudaGetSymbolAddress on the first call per device, and again only
+// when the device's current context is not the one of the last lookup.
 cudaError_t counts_on(int device, int32_t** out) {
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_counts_mu);
-  if (g_counts_addr[device] == nullptr) {
+  CountsAddr& c = g_counts_addr[device];
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx) == cudaSuccess;
+  if (c.ptr == nullptr || !have_ctx || ctx != c.ctx_id) {
     void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_plan_counts);
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_plan_counts);  // binds the device's context if need be
     if (e != cudaSuccess) return e;
-    g_counts_addr[device] = static_cast<int32_t*>(ptr);
+    if (!have_ctx && current_context_id(&ctx) != cudaSuccess) return cudaErrorDeviceUninitialized;
+    c.ptr = static_cast<int32_t*>(ptr);
+    c.ctx_id = ctx;
   }
-  *out = g_counts_addr[device];
+  *out = c.ptr;
   return cudaSuccess;
 }
 
@@ -62,7 +101,7 @@ __global__ void __launch_bounds__(kBlock) k_noalloc_count(DevPool p, const int32
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
-    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
+    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, 1, bits);
     if (b >= 0) atomicAdd(counts + b, 1);
   }
   if (bits) atomicOr(p.err, bits);
@@ -71,7 +110,7 @@ __global__ void __launch_bounds__(kBlock) k_noalloc_count(DevPool p, const int32
 // Counts -> start offsets (in place) and the plan header.
 __global__ void __launch_bounds__(kScanThreads) k_noalloc_scan(int64_t n_pages, int32_t n_seqs, int32_t max_pages,
                                                                int32_t* counts, int32_t* __restrict__ plan) {
-  scan_plan_counts(counts, n_pages, n_seqs, max_pages, plan);
+  scan_plan_counts(counts, n_pages, n_seqs, max_pages, 0, plan);
 }
 
 // Each entry takes the next position of its page; afterwards counts[b] is the
@@ -84,7 +123,7 @@ __global__ void __launch_bounds__(kBlock) k_noalloc_scatter(DevPool p, const int
   int bits = 0;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_entries; e += step) {
-    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, bits);
+    const int64_t b = plan_bucket(p, e, bt, max_pages, seq_start, seq_len, 1, bits);
     if (b >= 0) plan_place(entries, counts + b, n_entries, e, bits);
   }
   if (bits & KV_DEV_ERR_TABLE) atomicOr(p.err, KV_DEV_ERR_TABLE);

@@ -100,10 +100,14 @@ __global__ void __launch_bounds__(kBlock) k_store(DevPool p, int32_t layer0, int
         if (t < n_tasks) id = slot_to_id(p, id, v2p, v2p_len, bits);
       }
       if (t < n_tasks) {
-        if (id >= 0 && id < p.n_rows) {
-          row = id + (layer0 + l) * p.kv_rows * p.ps;
-        } else {
+        if (id < 0 || id >= p.n_rows) {
           atomicOr(p.err, KV_DEV_ERR_ROW);
+        } else if (!SLOTS && static_cast<uint32_t>(id) % static_cast<uint32_t>(p.stride) >= p.ps) {
+          // not of the form page * ps * 2L + o with o < ps: its rows would land
+          // in another layer's row-block, so the task is skipped
+          atomicOr(p.err, KV_DEV_ERR_FORM);
+        } else {
+          row = id + (layer0 + l) * p.kv_rows * p.ps;
         }
       }
     };

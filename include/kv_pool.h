@@ -33,9 +33,10 @@
  *    owns every buffer it passes.
  *  - Compute calls are asynchronous on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream), launch only this library's kernels, allocate
- *    nothing and never synchronize; all but kv_gather_plan_noalloc (see its
- *    own comment) can be captured in a CUDA graph. kv_pool_last_error is the
- *    one call that synchronizes.
+ *    nothing and never synchronize. kv_translate, kv_translate_mapped, the
+ *    stores, kv_translate_block_table, kv_gather_plan, kv_gather_plan_kf,
+ *    the gathers and kv_move can be captured in a CUDA graph.
+ *    kv_pool_last_error is the one call that synchronizes.
  *  - The calling thread's current device must be the pool's device.
  *  - Return value: KV_OK (0) or a negative KV_ERR_* code. These are argument,
  *    layout and launch errors, found on the host before anything is enqueued
@@ -79,7 +80,10 @@ enum {
 #define KV_DEV_ERR_V2P 2   /* translate: a virtual page index was past the page map        */
 #define KV_DEV_ERR_TABLE 4 /* gather: sequence metadata inconsistent (see kv_gather_layer);
                               plan: the table changed while the plan was built */
-#define KV_DEV_ERR_FORM 8  /* move: an id was not p * ps * 2L + o with o < ps; pair skipped */
+#define KV_DEV_ERR_FORM 8  /* store / move: an id was not p * ps * 2L + o with o < ps (token or
+                              pair skipped);
+                              kernel-facing gather / plan: an entry was not a multiple of 2L
+                              (its tokens skipped) */
 
 typedef struct kv_pool kv_pool_t; /* opaque, host-side, owned by the library */
 
@@ -200,8 +204,9 @@ int kv_translate_mapped(const kv_pool_t* pool, const int64_t* slots_dev, int64_t
  *  v_dev    [n, H, D] contiguous, R bytes per row, 16-byte aligned
  * Duplicate ids (tombstones all map to id 0, the sink) leave the row with
  * some mix of the duplicates' words: which one wins is unspecified.
- * Device errors: an id outside [0, n_rows) sets KV_DEV_ERR_ROW; its rows are
- * skipped. */
+ * Device errors: an id outside [0, n_rows) sets KV_DEV_ERR_ROW, and an id
+ * that kv_translate cannot produce (id % (ps*2L) >= ps, whose rows would land
+ * in another layer's row-block) sets KV_DEV_ERR_FORM; its rows are skipped. */
 int kv_store_layer(const kv_pool_t* pool, int32_t layer, const int32_t* ids_dev, int64_t n,
                    const void* k_dev, const void* v_dev, kv_stream_t stream);
 
@@ -209,7 +214,8 @@ int kv_store_layer(const kv_pool_t* pool, int32_t layer, const int32_t* ids_dev,
  * K_all[l] and V_all[l] as layer l's rows.
  * Source: the same assignment as kv_store_layer, over all 2L row-blocks of
  * the envelope (实现拆解 step 1).
- *  k_all_dev, v_all_dev  [L, n, H, D] contiguous (layer-major), 16-byte aligned */
+ *  k_all_dev, v_all_dev  [L, n, H, D] contiguous (layer-major), 16-byte aligned
+ * Device errors: as kv_store_layer. */
 int kv_store_all_layers(const kv_pool_t* pool, const int32_t* ids_dev, int64_t n, const void* k_all_dev,
                         const void* v_all_dev, kv_stream_t stream);
 
@@ -280,11 +286,13 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
  * kv_gather_plan: builds the plan into plan_dev (device, plan_bytes long,
  *   4-byte aligned; the caller owns it and may reuse it until the table
  *   changes). Layout (int32): [0] entries in the plan, [1] n_seqs,
- *   [2] max_pages, [3] 1 when the page-major order pays (entries >= 1.5 x
- *   distinct pages) else 0, then num_pages + 1 per-page offsets (the sort's
- *   workspace), then the entry indices s * max_pages + k grouped by page.
- *   With [3] = 0 (pages hardly shared) the planned gather keeps the table's
- *   own order, whose output writes stay sequential.
+ *   [2] max_pages, [3] flags: bit 0 set when the page-major order pays
+ *   (entries >= 1.5 x distinct pages), bit 1 set when the plan was built
+ *   from a kernel-facing table (kv_gather_plan_kf); then num_pages + 1
+ *   per-page offsets (the sort's workspace), then the entry indices
+ *   s * max_pages + k grouped by page. With bit 0 clear (pages hardly
+ *   shared) the planned gather keeps the table's own order, whose output
+ *   writes stay sequential.
  *   Only entries holding tokens of [start_s, len_s) enter the plan; an entry
  *   naming a page >= num_pages sets KV_DEV_ERR_ROW and is left out. The
  *   table must not change while the plan builds (it is read twice, to count
@@ -293,9 +301,10 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
  * kv_gather_layer_planned: kv_gather_layer with the same arguments plus the
  *   plan built from the same block table, starts and lengths (plan_bytes: the
  *   size of its buffer, at least kv_gather_plan_bytes(), else KV_ERR_INVALID);
- *   the output is identical. A plan built for another table shape sets
- *   KV_DEV_ERR_TABLE and writes nothing; plan entries are bounds-checked one
- *   by one, so a stale or foreign plan never reads outside its buffer. */
+ *   the output is identical. A plan built for another table shape, or from
+ *   a kernel-facing table, sets KV_DEV_ERR_TABLE and writes nothing; plan
+ *   entries are bounds-checked one by one, so a stale or foreign plan never
+ *   reads outside its buffer. */
 int kv_gather_plan_bytes(const kv_pool_t* pool, int32_t n_seqs, int32_t max_pages, int64_t* plan_bytes);
 int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
                    const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,
@@ -325,8 +334,9 @@ int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* pl
  * before anything is enqueued. The array (65537 int32 counters, 256 KiB + 4 B)
  * is held by every GPU that loads the library until the process exits.
  * Set-up: the first call on each device looks up the array's device address
- * with that device current (cudaGetSymbolAddress); make that first call
- * before any stream capture. Sharing: every call uses the same array, which
+ * with that device current (cudaGetSymbolAddress), and so does the first
+ * call after the device's context was created anew (cudaDeviceReset); make
+ * that first call before any stream capture. Sharing: every call uses the same array, which
  * keeps the previous call's contents; each call clears the counters it uses
  * on its stream first, so calls ordered on the GPU are independent, but calls
  * that overlap on the GPU (different streams, threads or pools on one device)
@@ -368,6 +378,46 @@ int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* ds
 int kv_translate_block_table(const kv_pool_t* pool, const int32_t* virt_bt_dev, int32_t n_seqs, int32_t max_pages,
                              const int32_t* seq_len_dev, const int32_t* v2p_dev, int64_t v2p_len,
                              int32_t* out_bt_dev, kv_stream_t stream);
+
+/* Gathers that read a kernel-facing block table directly: the table
+ * kv_translate_block_table writes, whose entry for a page is phys * 2L, so
+ * that entry * ps + o is the kernel-facing id of the token at offset o.
+ * Source: the report's read path builds this prefix-only kernel-facing page
+ * table once and reads through it (关联脉络, PR #35247), over
+ * translate_kv_loc_for_kernel's id form (关键源码片段
+ * multi_ended_allocator.py) and build_mha_views' dense views.
+ *
+ * kv_gather_layer_kf: kv_gather_layer with kf_table_dev in place of a
+ *   physical table: for sequence s and token j in [start_s, len_s),
+ *   e = kf_table[s * max_pages + j / ps] and the token's K and V rows are
+ *   those of kernel-facing id e * ps + j % ps, i.e. page e / 2L, offset
+ *   j % ps. A tombstoned virtual page (entry 0) therefore reads page 0, the
+ *   sink page, at the token's own offset; a negative entry (never written by
+ *   kv_translate_block_table) reads the sink row (page 0, offset 0) as in
+ *   kv_gather_layer. Entries past a sequence's window are never read, so the
+ *   prefix-only table suffices. Arguments, output layout and the other
+ *   device error bits are kv_gather_layer's. Device errors: an entry >=
+ *   num_pages * 2L sets KV_DEV_ERR_ROW and one that is not a multiple of 2L
+ *   sets KV_DEV_ERR_FORM; that entry's tokens are skipped (their output rows
+ *   are left untouched).
+ * kv_gather_plan_kf: kv_gather_plan over a kernel-facing table (entries
+ *   decoded as above; an off-grid entry sets KV_DEV_ERR_FORM and is left out
+ *   of the plan). The plan records its table form in flag bit 1.
+ * kv_gather_layer_planned_kf: kv_gather_layer_planned over a kernel-facing
+ *   table with a plan from kv_gather_plan_kf; a plan built from a physical
+ *   table sets KV_DEV_ERR_TABLE and writes nothing.
+ * In an MLA pool 2L reads L throughout. */
+int kv_gather_layer_kf(const kv_pool_t* pool, int32_t layer, const int32_t* kf_table_dev, int32_t n_seqs,
+                       int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
+                       const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,
+                       kv_stream_t stream);
+int kv_gather_plan_kf(const kv_pool_t* pool, const int32_t* kf_table_dev, int32_t n_seqs, int32_t max_pages,
+                      const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,
+                      kv_stream_t stream);
+int kv_gather_layer_planned_kf(const kv_pool_t* pool, int32_t layer, const void* plan_dev, int64_t plan_bytes,
+                               const int32_t* kf_table_dev, int32_t n_seqs, int32_t max_pages,
+                               const int32_t* seq_start_dev, const int32_t* seq_len_dev, const int64_t* cu_out_dev,
+                               void* out_k_dev, void* out_v_dev, int64_t out_rows, kv_stream_t stream);
 
 /* Read and clear the pool's device error word. Takes the word and zeroes it
  * in one atomic exchange, ordered on `stream` (one tiny kernel), synchronizes

@@ -3,7 +3,8 @@
 anchors, MLA pools, shared and tombstoned block-table entries, partial windows,
 empty sequences. Each case runs translate (with a page map), per-layer and
 all-layer stores, the table-order, planned and allocation-free-planned gathers,
-and a move, and compares every byte of the pool and of the outputs."""
+the kernel-facing table build and both gathers that read it, and a move, and
+compares every byte of the pool and of the outputs."""
 from __future__ import annotations
 
 import numpy as np
@@ -121,6 +122,32 @@ def test_random_geometry_matches_oracle(seed):
             else:
                 gt.kv_gather_layer_planned(pp.pool, layer, plan if how == "plan" else plan_na, to_dev(bt),
                                            to_dev(ln), to_dev(g.cu), dk, dv, to_dev(st))
+            assert pp.last_error() == 0
+            assert_bytes_equal(dk.cpu().numpy(), ok, f"{shape.name} gather K ({how}) layer {layer}", R)
+            if not latent:
+                assert_bytes_equal(dv.cpu().numpy(), ov, f"{shape.name} gather V ({how}) layer {layer}", R)
+
+    # the read path through a kernel-facing table: the same table read as
+    # virtual pages through the page map, prefix-only build, then both
+    # kernel-facing gathers
+    kf_ref, err = o.block_table_kf(bt, ln, v2p, out=np.full(bt.shape, -7, np.int32))
+    kf_d = torch.full(bt.shape, -7, dtype=torch.int32, device="cuda")
+    gt.kv_translate_block_table(pp.pool, to_dev(bt), to_dev(ln), to_dev(v2p), kf_d)
+    assert pp.last_error() == dev_bits(err)
+    assert np.array_equal(kf_d.cpu().numpy(), kf_ref)
+    plan_kf = gt.kv_gather_plan_kf(pp.pool, kf_d, to_dev(ln), to_dev(st))
+    assert pp.last_error() == 0
+    for layer in sorted(set(rng.integers(0, L, size=2).tolist())):
+        ok, ov, err = o.gather_kf(pp.M, layer, kf_ref, ln, g.cu, st, rows)
+        assert err == 0
+        for how in ("kf", "kf_plan"):
+            dk = torch.full((rows, R), 0x6B, dtype=torch.uint8, device="cuda")
+            dv = None if latent else torch.full((rows, R), 0x6B, dtype=torch.uint8, device="cuda")
+            if how == "kf":
+                gt.kv_gather_layer_kf(pp.pool, layer, kf_d, to_dev(ln), to_dev(g.cu), dk, dv, to_dev(st))
+            else:
+                gt.kv_gather_layer_planned_kf(pp.pool, layer, plan_kf, kf_d, to_dev(ln), to_dev(g.cu), dk, dv,
+                                              to_dev(st))
             assert pp.last_error() == 0
             assert_bytes_equal(dk.cpu().numpy(), ok, f"{shape.name} gather K ({how}) layer {layer}", R)
             if not latent:

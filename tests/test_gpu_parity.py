@@ -223,6 +223,24 @@ def test_error_paths_match_oracle():
     gt.kv_store_layer(pp.pool, 1, to_dev(bad), to_dev(K), to_dev(V))
     assert pp.last_error() == gt.KV_DEV_ERR_ROW
     assert_pool_matches(pp, M0, {})
+    # store: in-range ids that translate cannot produce (offset >= ps inside
+    # the page envelope) are skipped too, per-layer and all-layer
+    for form_bad in ([5, 21], [0, 30, 38]):
+        slots2 = synth.distinct_slots(rng, ps, P * ps, 40)
+        K2, V2 = _vals(shape, rng, (2, 40))
+        ids2, _ = o.translate(slots2)
+        bad2 = ids2.copy()
+        bad2[form_bad] += ps  # same page envelope, offset in [ps, 2 ps): another row-block
+        keep2 = np.ones(40, bool)
+        keep2[form_bad] = False
+        if len(form_bad) == 2:
+            o.store(pp.M, 0, slots2[keep2], K2[0][keep2], V2[0][keep2])
+            gt.kv_store_layer(pp.pool, 0, to_dev(bad2), to_dev(K2[0]), to_dev(V2[0]))
+        else:
+            o.store_all(pp.M, slots2[keep2], K2[:, keep2], V2[:, keep2])
+            gt.kv_store_all_layers(pp.pool, to_dev(bad2), to_dev(K2), to_dev(V2))
+        assert pp.last_error() == gt.KV_DEV_ERR_FORM
+        assert_pool_matches(pp, M0, {})
     # move: a non-translate-form id and an out-of-range id skip their pairs
     src, _ = o.translate(slots[:6])
     free = np.setdiff1d(np.arange(ps, P * ps), slots)[:6]
