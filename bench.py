@@ -47,19 +47,51 @@ WORKLOAD = ("llama3-8b-decode: L=32 H_kv=8 D=128 bf16 ps=16 P=4096 (8 GiB pool);
             "(store_layer 256 decode tokens + gather 256 seqs x 4096 tokens), move 8192 tokens x 64 row-blocks")
 
 
-def useful_bytes(shape=SHAPE, n_decode=N_DECODE, ctx=CTX, n_chunk=N_CHUNK, n_move=N_MOVE, n_seqs=None):
-    """Algorithmic bytes per step, by kernel (every row read once and written
-    once, plus the index bytes each kernel must read)."""
+def gather_bytes(g: synth.GatherBatch, ps: int, R: int, kv_rows: int = 2) -> dict:
+    """Bytes one gather launch of batch g moves, two ways.
+
+    method: what the gather must move at the least -- every distinct source
+    row the table names inside the windows read once (K and V), every output
+    row written once, plus the table entries that cover the windows and the
+    per-sequence start, length and output offset. This is the figure the HBM
+    roofline bounds.
+    per_reader: every output row's source counted once per reader (2R read +
+    2R written per output token, plus 4/ps of table): a page that many
+    sequences share is counted once per sequence, so this rate can exceed
+    the HBM peak when L2 serves the repeats."""
+    bt = np.asarray(g.block_table)
+    st = np.asarray(g.seq_start, np.int64)
+    ln = np.asarray(g.seq_len, np.int64)
+    cnt = np.maximum(ln - st, 0)
+    rows = int(cnt.sum())
+    seq = np.repeat(np.arange(bt.shape[0]), cnt)
+    j = np.arange(rows, dtype=np.int64) - np.repeat(np.cumsum(cnt) - cnt, cnt) + np.repeat(st, cnt)
+    page = bt[seq, j // ps].astype(np.int64)
+    tok = np.where(page < 0, -1, page * ps + j % ps)  # a tombstoned entry reads the one sink row
+    distinct = int(np.unique(tok).size) if rows else 0
+    first = st // ps
+    last = np.where(cnt > 0, -(-ln // ps), first)
+    entries = int(np.maximum(last - first, 0).sum())
+    method = distinct * kv_rows * R + rows * kv_rows * R + entries * 4 + bt.shape[0] * (4 + 4 + 8)
+    per_reader = rows * 2 * kv_rows * R + rows * 4 // ps
+    return {"method": method, "per_reader": per_reader, "rows": rows, "distinct_source_rows": distinct,
+            "table_entries": entries}
+
+
+def step_bytes(g: synth.GatherBatch, shape=SHAPE, n_decode=N_DECODE, n_chunk=N_CHUNK, n_move=N_MOVE):
+    """Method bytes of one step, by kernel (every row read once and written
+    once, plus the index bytes each kernel must read), and the per-launch
+    gather accounting (gather_bytes)."""
     L, R, ps = shape.layer_num, shape.row_bytes, shape.page_size
-    n_seqs = n_decode if n_seqs is None else n_seqs
-    rows = n_seqs * ctx
-    return {
+    gb = gather_bytes(g, ps, R)
+    by_kernel = {
         "translate": (n_decode + n_chunk) * (8 + 4),
         "store_all_layers": n_chunk * (2 * L * R * 2 + 4),
         "store_layer": L * n_decode * (2 * R * 2 + 4),
-        "gather": L * (rows * 4 * R + rows * 4 // ps),
+        "gather": L * gb["method"],
         "move": n_move * (2 * L * R * 2 + 8),
     }
+    return by_kernel, gb
 
 
 # ------------------------------------------------------------------ inputs
@@ -157,7 +189,9 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
-GATHER_SOURCES = [os.path.join(ROOT, "gather_translate_kv_gb300", "csrc", f) for f in ("kv_gather.cu", "kv_common.cuh")]
+GATHER_SOURCES = [os.path.join(ROOT, "gather_translate_kv_gb300", "csrc", f)
+                  for f in ("kv_gather.cu", "kv_common.cuh", "kv_plan.cuh")]
+TRAFFIC_PROFILE = "gather_planned_decode_small_dram.txt"
 
 
 def sources_hash(paths) -> str:
@@ -170,21 +204,26 @@ def sources_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(summary="gather_decode_llama3_8b.txt", sources=GATHER_SOURCES):
-    """DRAM bytes per gather launch from the committed ncu summary, or None when
-    the kernel's sources changed since the counters were taken."""
+def profiled_traffic(out_rows: int, summary=TRAFFIC_PROFILE, sources=GATHER_SOURCES):
+    """DRAM bytes of one planned decode gather launch of `out_rows` output rows:
+    the committed ncu summary of a small case with the same page sharing
+    (each page named ~16 times) gives DRAM bytes per output row, which is
+    scaled by the rows of the full launch. None when the summary is missing
+    or the kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", summary)
     try:
         text = open(path).read()
     except OSError:
         return None
-    src_hash = traffic = None
+    src_hash = per_row = None
     for line in text.splitlines():
         if line.startswith("kernel_sources_sha256_16:"):
             src_hash = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_launch:"):
-            traffic = float(line.split(":", 1)[1].strip())
-    return traffic if src_hash == sources_hash(sources) else None
+        if line.startswith("dram_bytes_per_output_row:"):
+            per_row = float(line.split(":", 1)[1].strip())
+    if per_row is None or src_hash != sources_hash(sources):
+        return None
+    return round(per_row * out_rows)
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -206,10 +245,12 @@ def cpu_model() -> str:
 
 def oracle_sample(budget_s: float = 12.0, threads: int = 1):
     """The oracle, as it stands, on a bounded sample of the step, repeated
-    until `budget_s` has elapsed. One sample: a 256-page pool of the same
+    until `budget_s` has elapsed. One sample: a 257-page pool of the same
     model shape; translate 512 slots; the 256-token all-layer store; 256
-    decode tokens stored for one layer; 32 sequences x 4096 tokens gathered
-    for one layer; 512 moved tokens. With threads > 1 the sample is split
+    decode tokens stored for one layer; 16 sequences x 4096 tokens gathered
+    for one layer, each through a permutation of the 256 allocatable pages
+    (so each page is named 16 times, as in the step); 512 moved tokens. Rates
+    count method bytes, as the GPU line does. With threads > 1 the sample is split
     across threads (gather by sequence, all-layer store by layer, the rest by
     token ranges), all on one shared pool mirror with disjoint writes; the
     oracle's C routines release the GIL."""
@@ -217,7 +258,7 @@ def oracle_sample(budget_s: float = 12.0, threads: int = 1):
 
     import oracle as ora
 
-    P, n_seq = 256, 32
+    P, n_seq = 257, 16  # 16 sequences x 256 pages of 256: each page named 16 times, as in the step
     sh = SHAPE.scaled(P)
     L = sh.layer_num
     o = ora.Oracle(ora.Geometry(L, sh.head_num, sh.head_dim, sh.itemsize, sh.page_size, P))
@@ -225,7 +266,7 @@ def oracle_sample(budget_s: float = 12.0, threads: int = 1):
     rng = synth.rng_for(sh.seed, synth.S_MISC, 1)
     ps, R = sh.page_size, sh.row_bytes
     slots = synth.distinct_slots(rng, ps, P * ps, 256 + 256 + 1024)
-    bt = rng.integers(1, P, size=(n_seq, CTX // ps)).astype(np.int32)
+    bt = np.stack([1 + rng.permutation(P - 1)[:CTX // ps] for _ in range(n_seq)]).astype(np.int32)
     kc, vc = synth.kv_pair(sh, L * 256, 1)
     kc, vc = kc.reshape(L, 256, -1), vc.reshape(L, 256, -1)
     kd, vd = synth.kv_pair(sh, 256, 0)
@@ -233,8 +274,9 @@ def oracle_sample(budget_s: float = 12.0, threads: int = 1):
     dst, _ = o.translate(slots[1024:])
     outk = np.empty((n_seq * CTX, R), np.uint8)
     outv = np.empty((n_seq * CTX, R), np.uint8)
-    per = useful_bytes(sh, n_decode=256, ctx=CTX, n_chunk=256, n_move=512, n_seqs=n_seq)
-    per_rep = per["translate"] + per["store_all_layers"] + per["store_layer"] // L + per["gather"] // L + per["move"]
+    g_all = synth.GatherBatch(bt, np.zeros(n_seq, np.int32), np.full(n_seq, CTX, np.int32))
+    per, gb = step_bytes(g_all, sh, n_decode=256, n_chunk=256, n_move=512)
+    per_rep = per["translate"] + per["store_all_layers"] + per["store_layer"] // L + gb["method"] + per["move"]
 
     def rng_of(n, w):
         k = -(-n // threads)
@@ -265,9 +307,10 @@ def oracle_sample(budget_s: float = 12.0, threads: int = 1):
             if el >= budget_s:
                 break
     return {"value": per_rep * reps / el / GB, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": (f"{reps} reps on {threads} thread(s) of: a 256-page pool of the same shape; translate 512 "
-                       f"slots; store_all 256 tokens x 32 layers; store_layer 256 tokens; gather 32 seqs x 4096 "
-                       f"tokens for one layer; move 512 tokens; {el:.1f} s"),
+            "sample": (f"{reps} reps on {threads} thread(s) of: a 257-page pool of the same shape; translate 512 "
+                       f"slots; store_all 256 tokens x 32 layers; store_layer 256 tokens; gather {n_seq} seqs x 4096 "
+                       f"tokens for one layer (each table a permutation of pages 1..256: each page named 16 times); "
+                       f"move 512 tokens; method bytes; {el:.1f} s"),
             "cpu_model": cpu_model(), "seconds": el}
 
 
@@ -350,6 +393,33 @@ def make_step(gt, pool, inp, dev, stream) -> Step:
 
 
 
+TARGETS = ["store:3", "store_all:3", "move:2", "move:4"]
+TARGET_NAMES = {"store:3": "store_layer, llama3-8b-prefill (32768 tokens per layer, 2 % tombstones)",
+                "store_all:3": "store_all_layers, llama3-8b-prefill ([32, 32768, 8, 128] bf16, 4 GiB)",
+                "move:2": "move, llama3-8b-decode pool (8192 tokens x 64 row-blocks x 2 KiB)",
+                "move:4": "move, swa-fp8 pool (8192 tokens x 48 row-blocks x 512 B)"}
+
+
+def run_targets(iters: int) -> dict:
+    """The store and move workloads graded beside the gather, each timed per
+    launch with CUDA events (mean over `iters` launches after 3 warm-ups; L2
+    flushed before each launch whose working set is under 4x L2), on its own
+    pool, freed afterwards."""
+    ns = argparse.Namespace(iters=iters, torch_ref=0, pages=0, layers=0, seqs=0, only=",".join(TARGETS))
+    out = {}
+    for rec in run_micro(ns, quiet=True):
+        if rec.get("micro") == "skipped":
+            out[f"skipped_cfg{rec['cfg']}"] = rec["reason"]
+            continue
+        key = {"store_layer": "store", "store_all_layers": "store_all", "move": "move"}[rec["micro"]]
+        key = f"{key}:{rec['cfg']}"
+        out[key] = {"what": TARGET_NAMES[key], "us_per_call": rec["us_per_call"],
+                    "method_bytes_per_call": rec["useful_bytes_per_call"], "GBps": rec["useful_GBps"],
+                    "frac": round(rec["pct_of_hbm_peak"] / 100, 4), "calls": rec["calls"],
+                    "l2_flush": rec.get("l2_flush")}
+    return out
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -415,47 +485,58 @@ def run_gpu(args):
     gather_ms = statistics.mean(a.elapsed_time(b) for a, b in gather_ev)
     dev_err = gt.kv_pool_last_error(pool)
 
-    # end to end: pinned host inputs -> device every step, ids + error word back
+    # end to end, through the public API: pinned host inputs -> device every
+    # step, and the step's product -> pinned host memory: the last layer's
+    # gathered K and V (4 GiB), the translated ids and the device error word
     host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in
             dict(slots=inp["slots"], bt=g.block_table, ln=g.seq_len, cu=g.cu, k_dec=inp["k_dec"],
                  v_dec=inp["v_dec"], k_chunk=inp["k_chunk"], v_chunk=inp["v_chunk"]).items()}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     ids_host = torch.empty(ids.shape, dtype=ids.dtype).pin_memory()
-    d2h = ids_host.numel() * 4 + 4
+    out_k_host = torch.empty(st.out_k.shape, dtype=torch.uint8).pin_memory()
+    out_v_host = torch.empty(st.out_v.shape, dtype=torch.uint8).pin_memory()
+    d2h_small = ids_host.numel() * 4 + 4
+    d2h = d2h_small + out_k_host.numel() + out_v_host.numel()
     stage = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
 
-    def e2e_step():
+    def e2e_step(read_result: bool):
         for k, v in host.items():
             stage[k].copy_(v, non_blocking=True)
         step(stage)
         ids_host.copy_(ids, non_blocking=True)
+        if read_result:
+            out_k_host.copy_(st.out_k, non_blocking=True)
+            out_v_host.copy_(st.out_v, non_blocking=True)
         return gt.kv_pool_last_error(pool, stream)  # synchronizes: the step's result is on the host
 
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    t0 = time.perf_counter()
-    e2e_steps = max(3, args.steps // 2)
+    e2e_s = {}
     bad = 0
-    for _ in range(e2e_steps):
-        bad |= e2e_step()
-    barrier()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    for read_result in (True, False):
+        for _ in range(2):
+            e2e_step(read_result)
+        barrier()
+        t0 = time.perf_counter()
+        e2e_steps = max(3, args.steps // 2)
+        for _ in range(e2e_steps):
+            bad |= e2e_step(read_result)
+        barrier()
+        e2e_s[read_result] = (time.perf_counter() - t0) / e2e_steps
 
-    ub = useful_bytes()
-    step_bytes = sum(ub.values())
-    ms, e2e_ms, gather_ms = reduce_max([ms, e2e_s * 1e3, gather_ms], dev)
+    sb, gb = step_bytes(g)
+    step_total = sum(sb.values())
+    per_reader_total = step_total - sb["gather"] + L * gb["per_reader"]
+    ms, e2e_ms, e2e_nr_ms, gather_ms = reduce_max([ms, e2e_s[True] * 1e3, e2e_s[False] * 1e3, gather_ms], dev)
+    del stage, host, out_k_host, out_v_host
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
     peak, peak_kind = measured_hbm_peak()
-    gather_bytes = ub["gather"] / L
-    achieved = gather_bytes / (gather_ms * 1e-3) / GB
-    traffic = profiled_traffic()
+    achieved = gb["method"] / (gather_ms * 1e-3) / GB
+    traffic = profiled_traffic(gb["rows"])
     line = {
         "metric": "KV store/gather/move useful GB/s and % of GB300 HBM peak (byte-exact vs oracle)",
-        "value": round(whole_job_gbps(step_bytes, world, ms), 1),
+        "value": round(whole_job_gbps(step_total, world, ms), 1),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -466,24 +547,45 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "u8",
         "data": "synthetic (seeded: bf16 N(0,1) K/V, random block tables and slots)",
-        "config": {"workload": WORKLOAD, "kv_dtype": "bf16", "useful_bytes_per_step": step_bytes,
-                   "useful_bytes_by_kernel": ub, "l2": "no flush: inputs larger than L2 (8 GiB pool, "
-                   "4 GiB gather output per layer)", "parallelism": f"replicas x{world}",
-                   "pct_of_hbm_peak": round(100 * step_bytes / (ms * 1e-3) / GB / peak, 1)},
-        "roofline": {"bound": "hbm", "kernel": "kv_gather_layer_planned", "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": gather_bytes, "avg_launch_ms": round(gather_ms, 4),
-                     # useful bytes count a shared page once per reader; DRAM moves it about once
-                     # (L2 serves the rest), so the DRAM-side rate is the one bounded by the peak
+        "config": {"workload": WORKLOAD, "kv_dtype": "bf16",
+                   "useful_bytes": "method bytes: each distinct source row read once, each output row "
+                                   "written once, plus index bytes",
+                   "useful_bytes_per_step": step_total, "useful_bytes_by_kernel": sb,
+                   "gather_per_launch": gb,
+                   "l2": "no flush: inputs larger than L2 (8 GiB pool, 4 GiB gather output per layer)",
+                   "parallelism": f"replicas x{world}",
+                   "pct_of_hbm_peak": round(100 * step_total / (ms * 1e-3) / GB / peak, 1),
+                   # every output row's source counted once per sequence that reads it; L2 serves the
+                   # repeats, so this rate is not bounded by the HBM peak
+                   "effective_GBps_per_reader": round(whole_job_gbps(per_reader_total, world, ms), 1),
+                   "useful_bytes_per_output_reference": per_reader_total},
+        "roofline": {"bound": "hbm", "kernel": "kv_gather_layer_planned (k_gather_runs<8, true, true>)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": gb["method"],
+                     "avg_launch_ms": round(gather_ms, 4),
                      "dram_achieved": None if traffic is None else round(traffic / (gather_ms * 1e-3) / GB, 1),
                      "dram_frac": None if traffic is None else round(traffic / (gather_ms * 1e-3) / GB / peak, 4)},
-        "e2e": {"value": round(whole_job_gbps(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": round(whole_job_gbps(step_total, world, e2e_ms), 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                "result": "the last layer's gathered K and V, the translated ids and the device error word",
+                "without_result_readback": {"value": round(whole_job_gbps(step_total, world, e2e_nr_ms), 1),
+                                            "d2h_bytes_per_step": d2h_small, "ms_per_step": round(e2e_nr_ms, 3)}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "device_errors": dev_err | bad,
     }
+    # the graded store and move workloads, after the step's pool is gone
+    del st, dev_in, ids, gather_ev
+    gt.kv_pool_destroy(pool)
+    del raw
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_targets:
+        clocks = ClockSampler(uuid)
+        clocks.start()
+        targets = run_targets(max(20, args.target_iters))
+        targets["clocks"] = clocks.stop()
+        line["targets"] = targets
     if world == 1 and not args.no_cpu_baseline:
         one = oracle_sample(args.cpu_budget / 2, 1)
         ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
@@ -549,12 +651,12 @@ def _payload_torch(gen, rows: int, R: int, itemsize: int, dev):
     return x.to(torch.uint8)
 
 
-def run_micro(args):
+def run_micro(args, quiet: bool = False) -> list[dict]:
     """Each kernel on each workload of the build plan, timed per launch with
     CUDA events (median), L2 flushed between launches whose working set is
     under 4x the L2 size (a 2x-L2 write followed by a 2x-L2 read, so the
     launch finds neither its data nor dirty lines in L2). One JSON line per
-    (kernel, workload)."""
+    (kernel, workload), printed unless `quiet`; the records are returned."""
     import torch
 
     import gather_translate_kv_gb300 as gt
@@ -576,6 +678,12 @@ def run_micro(args):
         flush_read.max()
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234)
+    records: list[dict] = []
+
+    def emit(line):
+        records.append(line)
+        if not quiet:
+            print(json.dumps(line), flush=True)
     stream = torch.cuda.current_stream(dev)
     todo = args.only.split(",") if args.only else MICRO_DEFAULT
     by_cfg: dict[int, list[str]] = {}
@@ -613,7 +721,7 @@ def run_micro(args):
             line["torch_indexing_us"] = round(r * 1e3, 2)
             line["speedup_vs_torch_indexing"] = round(r / med, 2)
         line.update(extra or {})
-        print(json.dumps(line), flush=True)
+        emit(line)
 
     if "ceiling" in by_cfg.pop(0, []):
         # context for the HBM-bound kernels: torch's own fill, copy and
@@ -647,7 +755,7 @@ def run_micro(args):
         total, pad = gt.kv_pool_required_bytes(desc)
         free, _ = torch.cuda.mem_get_info(dev)
         if total + pad + (8 << 30) > free:
-            print(json.dumps({"micro": "skipped", "cfg": cfg, "reason": f"{free / 2**30:.1f} GiB free"}))
+            emit({"micro": "skipped", "cfg": cfg, "reason": f"{free / 2**30:.1f} GiB free"})
             continue
         raw = torch.empty(total + pad, dtype=torch.uint8, device=dev)
         synth.fill_sentinel_torch(raw, 99)
@@ -751,12 +859,14 @@ def run_micro(args):
             ok = torch.empty((rows, R), dtype=torch.uint8, device=dev)
             ov = None if sh.latent else torch.empty_like(ok)
             bt, ln, cu, st = d(gb.block_table), d(gb.seq_len), d(gb.cu), d(gb.seq_start)
-            useful = rows * 2 * kvr * R + rows * 4 // ps
-            flush = useful < 4 * l2
+            acct = gather_bytes(gb, ps, R, kvr)
+            useful = acct["method"]  # distinct source rows once, output rows once, index bytes
+            flush = acct["per_reader"] < 4 * l2
             layers = list(range(L)) if cfg != 5 else [0, L - 1]
             distinct = len(np.unique(gb.block_table))
             share = {"l2_flush": flush, "distinct_pages": distinct,
-                     "page_reads_per_distinct_page": round(gb.block_table.size / max(1, distinct), 2)}
+                     "page_reads_per_distinct_page": round(gb.block_table.size / max(1, distinct), 2),
+                     "per_reader_bytes_per_call": acct["per_reader"]}
             if "gather_planned" in kernels:
                 plan = gt.kv_gather_plan(pool, bt, ln, st)
                 ms = timed(lambda i: gt.kv_gather_layer_planned(pool, layers[i % len(layers)], plan, bt, ln, cu, ok,
@@ -812,6 +922,147 @@ def run_micro(args):
         gt.kv_pool_destroy(pool)
         del raw
         torch.cuda.empty_cache()
+    del flush_buf, flush_read
+    torch.cuda.empty_cache()
+    return records
+
+
+# ------------------------------------------------------------------ CPU baseline table
+
+CPU_TABLE = {  # cfg: (oracle pool pages, store tokens, gather seqs, gather pages per seq, window, move pairs)
+    1: (64, 100, 1, 8, None, 20),
+    2: (64, 256, 16, 63, None, 256),
+    3: (32, 1984, 1, 31, None, 0),
+    4: (256, 512, 50, 5, 128, 512),
+    5: (64, 14000, 64, 4, None, 512),
+}
+CPU_KERNELS = ("translate", "store_layer", "store_all_layers", "gather_layer", "move")
+
+
+def _cpu_cases(cfg: int):
+    """Oracle inputs for one workload, on a pool of the workload's model shape
+    with fewer pages (the full pools are 8 to 119 GiB): tokens at distinct
+    random slots outside page 0 (no tombstones, so that threads write disjoint
+    rows), K/V bytes, block tables whose sequences take random distinct pages,
+    and disjoint move pairs."""
+    import oracle as ora
+
+    sh = synth.SHAPES[cfg]
+    P, n, S_, npg, win, m = CPU_TABLE[cfg]
+    sh = sh.scaled(P)
+    ps, R, L = sh.page_size, sh.row_bytes, sh.layer_num
+    o = ora.Oracle(ora.Geometry(L, sh.head_num, sh.head_dim, sh.itemsize, ps, P))
+    rng = synth.rng_for(sh.seed, synth.S_MISC, 11)
+    slots = synth.distinct_slots(rng, ps, P * ps, n + 2 * m)
+    K = rng.integers(0, 256, size=(L, n, R), dtype=np.uint8)
+    V = rng.integers(0, 256, size=(L, n, R), dtype=np.uint8)
+    bt = np.stack([1 + rng.permutation(P - 1)[:npg] for _ in range(S_)]).astype(np.int32)
+    if win is None:
+        st = np.zeros(S_, np.int32)
+        ln = np.full(S_, npg * ps, np.int32)
+    else:
+        ln = (win + rng.integers(0, npg * ps - win + 1, size=S_)).astype(np.int32)
+        st = (ln - win).astype(np.int32)
+    g = synth.GatherBatch(bt, st, ln)
+    ids, _ = o.translate(slots[n:])
+    return dict(sh=sh, o=o, slots=slots[:n], K=K, V=V, g=g, src=ids[:m], dst=ids[m:], m=m, n=n)
+
+
+def _time_cpu(fn, units: int, threads: int, budget_s: float) -> float:
+    """Seconds per pass of fn over `units` units split in `threads` ranges."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    def ranges():
+        k = -(-units // threads)
+        return [(w * k, min(units, (w + 1) * k)) for w in range(threads) if w * k < units]
+
+    parts = ranges()
+    reps = 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            list(ex.map(lambda r: fn(*r), parts))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                return el / reps
+
+
+def run_cpu_table(args):
+    """The oracle, as it stands, per kernel and per workload, on one host
+    thread and on every host thread, in method bytes per second (the bytes
+    the GPU rows count). With a GPU, the library's --micro rate for the same
+    kernel and workload is printed beside it. One JSON line per cell, then a
+    markdown table."""
+    import oracle as ora
+
+    ora.build()
+    ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    gpu = {}
+    if not args.no_gpu:
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                items = [f"{k}:{c}" for c in CPU_TABLE for k in ("translate", "store", "store_all", "gather", "move")
+                         if not (k == "move" and CPU_TABLE[c][5] == 0)]
+                ns = argparse.Namespace(iters=args.iters, torch_ref=0, pages=0, layers=0, seqs=0, only=",".join(items))
+                for rec in run_micro(ns, quiet=True):
+                    if rec.get("micro") != "skipped":
+                        gpu[(rec["micro"], rec["cfg"])] = rec
+        except Exception as e:  # the table is still useful without the GPU column
+            print(json.dumps({"cpu_table": "gpu column skipped", "why": repr(e)[:200]}), flush=True)
+    rows = []
+    for cfg in sorted(CPU_TABLE):
+        c = _cpu_cases(cfg)
+        o, sh, n, m, g = c["o"], c["sh"], c["n"], c["m"], c["g"]
+        L, R, ps = sh.layer_num, sh.row_bytes, sh.page_size
+        M = synth.sentinel_bytes(3, 0, o.raw_bytes())
+        outk = np.empty((g.total, R), np.uint8)
+        outv = np.empty((g.total, R), np.uint8)
+        gacct = gather_bytes(g, ps, R)
+
+        def translate(a, b):
+            o.translate(c["slots"][a:b])
+
+        def store(a, b):
+            o.store(M, L - 1, c["slots"][a:b], c["K"][0, a:b], c["V"][0, a:b])
+
+        def store_all(a, b):
+            for layer in range(a, b):
+                o.store(M, layer, c["slots"], c["K"][layer], c["V"][layer])
+
+        def gather(a, b):
+            sub = synth.GatherBatch(g.block_table[a:b], g.seq_start[a:b], g.seq_len[a:b])
+            o.gather(M, L - 1, sub.block_table, sub.seq_len, sub.cu + g.cu[a], sub.seq_start, g.total, outk, outv)
+
+        def move(a, b):
+            o.move(M, c["src"][a:b], c["dst"][a:b])
+
+        cases = [("translate", translate, n, n * 12), ("store_layer", store, n, n * (4 * R + 4)),
+                 ("store_all_layers", store_all, L, L * n * 4 * R + n * 4),
+                 ("gather_layer", gather, g.block_table.shape[0], gacct["method"])]
+        if m:
+            cases.append(("move", move, m, m * (2 * L * R * 2 + 8)))
+        for name, fn, units, nbytes in cases:
+            t1 = _time_cpu(fn, units, 1, args.cpu_cell_s)
+            tn = _time_cpu(fn, units, ncores, args.cpu_cell_s)
+            rec = {"cpu_table": name, "cfg": cfg, "oracle_pool_pages": sh.num_pages, "units": units,
+                   "method_bytes": nbytes, "cpu_1t_GBps": round(nbytes / t1 / GB, 3),
+                   "cpu_nt_GBps": round(nbytes / tn / GB, 3), "threads": ncores, "cpu_model": cpu_model()}
+            gkey = {"gather_layer": "gather_layer_planned"}.get(name, name)
+            if (gkey, cfg) in gpu:
+                rec["gpu_GBps"] = gpu[(gkey, cfg)]["useful_GBps"]
+                rec["gpu_pct_of_hbm_peak"] = gpu[(gkey, cfg)]["pct_of_hbm_peak"]
+            print(json.dumps(rec), flush=True)
+            rows.append(rec)
+    print()
+    print(f"| Kernel | Config | GPU useful GB/s | % HBM peak | CPU 1-thread GB/s | CPU {ncores}-thread GB/s |")
+    print("|---|---|---|---|---|---|")
+    for r in rows:
+        gp = r.get("gpu_GBps")
+        print(f"| {r['cpu_table']} | {r['cfg']} | {gp if gp is not None else '-'} | "
+              f"{r.get('gpu_pct_of_hbm_peak', '-')} | {r['cpu_1t_GBps']} | {r['cpu_nt_GBps']} |")
 
 
 def main():
@@ -822,6 +1073,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-targets", action="store_true", help="skip the store / move target workloads")
+    ap.add_argument("--target-iters", type=int, default=20)
     ap.add_argument("--micro", action="store_true", help="per-kernel table instead of the step")
     ap.add_argument("--only", default="", help="micro entries, e.g. gather:2,move:4")
     ap.add_argument("--iters", type=int, default=50)
@@ -829,7 +1082,13 @@ def main():
     ap.add_argument("--pages", type=int, default=0, help="micro: override the page count")
     ap.add_argument("--layers", type=int, default=0, help="micro: override the layer count")
     ap.add_argument("--seqs", type=int, default=0, help="micro: gather only the first N sequences")
+    ap.add_argument("--cpu-table", action="store_true", help="the oracle per kernel and workload (CPU baseline)")
+    ap.add_argument("--cpu-cell-s", type=float, default=0.6, help="cpu-table: seconds per cell and thread count")
+    ap.add_argument("--no-gpu", action="store_true", help="cpu-table: leave out the GPU column")
     args = ap.parse_args()
+    if args.cpu_table:
+        run_cpu_table(args)
+        return
     if args.micro:
         run_micro(args)
         return
