@@ -128,20 +128,45 @@ class Full:
             exp[hit] = srows[order[pos[hit]]]
         return exp
 
-    def check_gather(self, layer, gb: synth.GatherBatch, stored: list, planned: bool = False):
+    def check_gather(self, layer, gb: synth.GatherBatch, stored: list, planned: bool = False,
+                     kernel_facing: bool = False):
         """Gather one layer (table order, or through a page-major plan) and
-        compare every output row with the oracle's source offsets."""
-        ks, vs, err = self.o.gather_rows(layer, gb.block_table, gb.seq_len, gb.cu, gb.seq_start)
-        assert err == 0 and (ks >= 0).all()
+        compare every output row with the oracle's source offsets. With
+        kernel_facing, the same physical pages are reached through a virtual
+        table and a random page map: the library builds the kernel-facing
+        table (checked against the oracle's) and gathers through it."""
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
         ok = torch.empty((gb.total, self.R), dtype=torch.uint8, device="cuda")
         ov = torch.empty_like(ok)
-        bt, ln, cu, st = d(gb.block_table), d(gb.seq_len), d(gb.cu), d(gb.seq_start)
-        if planned:
-            plan = gt.kv_gather_plan(self.pool, bt, ln, st)
-            gt.kv_gather_layer_planned(self.pool, layer, plan, bt, ln, cu, ok, ov, st)
+        ln, cu, st = d(gb.seq_len), d(gb.cu), d(gb.seq_start)
+        if kernel_facing:
+            P = self.shape.num_pages
+            rng = np.random.default_rng(4321 + layer)
+            v2p = np.zeros(P, np.int32)
+            v2p[1:] = 1 + rng.permutation(P - 1)  # a bijection of pages 1..P-1
+            inv = np.zeros(P, np.int32)
+            inv[v2p] = np.arange(P, dtype=np.int32)
+            virt = np.where(gb.block_table < 0, -1, inv[np.maximum(gb.block_table, 0)]).astype(np.int32)
+            kf_ref, err = self.o.block_table_kf(virt, gb.seq_len, v2p, out=np.zeros_like(virt))
+            assert err == 0
+            ks, vs, err = self.o.gather_rows(layer, kf_ref, gb.seq_len, gb.cu, gb.seq_start, kernel_facing=True)
+            kf = torch.zeros(virt.shape, dtype=torch.int32, device="cuda")
+            gt.kv_translate_block_table(self.pool, d(virt), ln, d(v2p), kf)
+            assert torch.equal(kf, d(kf_ref)), "kernel-facing table differs"
+            if planned:
+                plan = gt.kv_gather_plan_kf(self.pool, kf, ln, st)
+                gt.kv_gather_layer_planned_kf(self.pool, layer, plan, kf, ln, cu, ok, ov, st)
+            else:
+                gt.kv_gather_layer_kf(self.pool, layer, kf, ln, cu, ok, ov, st)
         else:
-            gt.kv_gather_layer(self.pool, layer, bt, ln, cu, ok, ov, st)
+            ks, vs, err = self.o.gather_rows(layer, gb.block_table, gb.seq_len, gb.cu, gb.seq_start)
+            bt = d(gb.block_table)
+            if planned:
+                plan = gt.kv_gather_plan(self.pool, bt, ln, st)
+                gt.kv_gather_layer_planned(self.pool, layer, plan, bt, ln, cu, ok, ov, st)
+            else:
+                gt.kv_gather_layer(self.pool, layer, bt, ln, cu, ok, ov, st)
+        assert err == 0 and (ks >= 0).all()
         assert gt.kv_pool_last_error(self.pool) == 0
         assert torch.equal(ok, self.expected_reads(ks, stored[0])), f"gathered K of layer {layer} differs"
         assert torch.equal(ov, self.expected_reads(vs, stored[1])), f"gathered V of layer {layer} differs"
@@ -154,7 +179,8 @@ def _vals(shape, n, layer, seed_extra=0):
 def test_decode_llama3_8b_full():
     """Workload 2 (8 GiB pool): gathers of 256 x 4096 tokens on the fresh
     pool, the per-layer decode store for all 32 layers, gathers that read the
-    new tokens, and the 8192-token move."""
+    new tokens (through physical and kernel-facing tables, in table and
+    page-major order), and the 8192-token move."""
     sh = synth.SHAPES[2]
     F = Full(sh)
     gb = synth.gather_batch(sh)
@@ -169,6 +195,9 @@ def test_decode_llama3_8b_full():
     for layer in (0, 17, 31):
         F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]))
         F.check_gather(layer, gb, ([stored[layer][0]], [stored[layer][1]]), planned=True)
+    # the same gathers read through kernel-facing tables
+    F.check_gather(5, gb, ([stored[5][0]], [stored[5][1]]), kernel_facing=True)
+    F.check_gather(31, gb, ([stored[31][0]], [stored[31][1]]), planned=True, kernel_facing=True)
     # move 8192 never-stored tokens to other never-stored tokens
     used = np.unique(np.concatenate([synth.store_slots(sh, l) for l in range(sh.layer_num)]))
     src, dst = synth.move_slots(sh, 8192, avoid=used)
@@ -219,7 +248,8 @@ def test_prefill_llama3_8b_full():
 def test_swa_fp8_full():
     """Workload 4 (12 GiB fp8 pool): for each of the 24 layers, store one
     token per sequence at position c-1 and gather the 128-token window
-    [c-128, c) of all 512 sequences; then the 8192-token move."""
+    [c-128, c) of all 512 sequences (every third layer through a
+    kernel-facing table); then the 8192-token move."""
     sh = synth.SHAPES[4]
     F = Full(sh)
     slots, gb = synth.swa_batch(sh)
@@ -227,7 +257,7 @@ def test_swa_fp8_full():
     for layer in range(sh.layer_num):
         K, V = _vals(sh, slots.size, layer)
         kd, vd, Kd, Vd = F.check_store(layer, slots, K, V, ids)
-        F.check_gather(layer, gb, ([(kd, Kd)], [(vd, Vd)]), planned=layer % 2 == 1)
+        F.check_gather(layer, gb, ([(kd, Kd)], [(vd, Vd)]), planned=layer % 2 == 1, kernel_facing=layer % 3 == 2)
     used = np.unique(gb.block_table.astype(np.int64)[:, :, None] * sh.page_size + np.arange(sh.page_size))
     src, dst = synth.move_slots(sh, 8192, avoid=used)
     src = np.setdiff1d(src, used)[:8000]
