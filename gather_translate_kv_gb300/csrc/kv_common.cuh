@@ -13,6 +13,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "kv_layout.h"
 #include "kv_pool.h"
 
@@ -247,16 +251,21 @@ inline cudaError_t dispatch_row(int64_t vpr, F&& f) {
   }
 }
 
-// Blocks per SM a kernel reaches at kBlock threads (cached per instantiation).
+// Blocks per SM a kernel reaches at kBlock threads, looked up once per kernel.
+// The cache is keyed by the kernel's address: the instances of one template
+// share a function-pointer type but not their register counts.
 template <class K>
 inline int blocks_per_sm(K kernel) {
-  static int cached = 0;
-  if (cached == 0) {
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kBlock, 0) != cudaSuccess || nb < 1) nb = 1;
-    cached = nb;
-  }
-  return cached;
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> cache;
+  const void* key = reinterpret_cast<const void*>(kernel);
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& e : cache)
+    if (e.first == key) return e.second;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kBlock, 0) != cudaSuccess || nb < 1) nb = 1;
+  cache.emplace_back(key, nb);
+  return nb;
 }
 
 // Grid for `warps_needed` warps of work, capped at one full wave of resident
