@@ -5,7 +5,9 @@
  *   c_abi_roundtrip        host-only checks: sizes and start-up gates
  *   c_abi_roundtrip gpu    + a translate -> store -> gather round trip on the
  *                          current device, with the library owning the pool,
- *                          and the same gather through a page-major plan
+ *                          the same gather through a page-major plan, and
+ *                          through a kernel-facing table built from virtual
+ *                          pages and a page map
  *
  * Pool: 2 layers, 2 KV heads, head_dim 8, bf16 (R = 32 bytes), page size 4,
  * 64 pages. Exit status 0 = every check passed.
@@ -133,6 +135,42 @@ static int gpu_roundtrip(void) {
   cudaMemcpy(gk, d_gk, sizeof gk, cudaMemcpyDeviceToHost);
   cudaMemcpy(gv, d_gv, sizeof gv, cudaMemcpyDeviceToHost);
   if (memcmp(gk, k, sizeof k) != 0 || memcmp(gv, v, sizeof v) != 0) return fail("planned round trip bytes", 0);
+
+  /* the read path through a kernel-facing table: virtual pages 0..3 map to
+   * the physical pages above; the table build writes phys * 2L = phys * 4 */
+  int32_t virt[PAGES] = {0, 1, 2, 3}, v2p[PAGES] = {7, 3, 12, 40}, kf[PAGES];
+  int32_t *d_virt, *d_v2p, *d_kf;
+  if (cudaMalloc((void**)&d_virt, sizeof virt) || cudaMalloc((void**)&d_v2p, sizeof v2p) ||
+      cudaMalloc((void**)&d_kf, sizeof kf))
+    return fail("cudaMalloc kf", 0);
+  cudaMemcpy(d_virt, virt, sizeof virt, cudaMemcpyHostToDevice);
+  cudaMemcpy(d_v2p, v2p, sizeof v2p, cudaMemcpyHostToDevice);
+  if ((rc = kv_translate_block_table(pool, d_virt, 1, PAGES, d_len, d_v2p, PAGES, d_kf, NULL)) != KV_OK)
+    return fail("kernel-facing table", rc);
+  cudaMemcpy(kf, d_kf, sizeof kf, cudaMemcpyDeviceToHost);
+  for (int i = 0; i < PAGES; ++i)
+    if (kf[i] != table[i] * 4) return fail("kernel-facing entry", kf[i]);
+  cudaMemset(d_gk, 0, sizeof gk);
+  cudaMemset(d_gv, 0, sizeof gv);
+  if ((rc = kv_gather_layer_kf(pool, 1, d_kf, 1, PAGES, NULL, d_len, d_cu, d_gk, d_gv, N, NULL)) != KV_OK)
+    return fail("kernel-facing gather", rc);
+  cudaMemcpy(gk, d_gk, sizeof gk, cudaMemcpyDeviceToHost);
+  cudaMemcpy(gv, d_gv, sizeof gv, cudaMemcpyDeviceToHost);
+  if (memcmp(gk, k, sizeof k) != 0 || memcmp(gv, v, sizeof v) != 0) return fail("kernel-facing round trip", 0);
+  cudaMemset(d_gk, 0, sizeof gk);
+  cudaMemset(d_gv, 0, sizeof gv);
+  if ((rc = kv_gather_plan_kf(pool, d_kf, 1, PAGES, NULL, d_len, d_plan, plan_bytes, NULL)) != KV_OK)
+    return fail("kernel-facing plan", rc);
+  if ((rc = kv_gather_layer_planned_kf(pool, 1, d_plan, plan_bytes, d_kf, 1, PAGES, NULL, d_len, d_cu, d_gk, d_gv,
+                                       N, NULL)) != KV_OK)
+    return fail("planned kernel-facing gather", rc);
+  if ((rc = kv_pool_last_error(pool, NULL, &bits)) != KV_OK || bits != 0) return fail("device errors (kf)", bits);
+  cudaMemcpy(gk, d_gk, sizeof gk, cudaMemcpyDeviceToHost);
+  cudaMemcpy(gv, d_gv, sizeof gv, cudaMemcpyDeviceToHost);
+  if (memcmp(gk, k, sizeof k) != 0 || memcmp(gv, v, sizeof v) != 0) return fail("planned kf round trip", 0);
+  cudaFree(d_virt);
+  cudaFree(d_v2p);
+  cudaFree(d_kf);
   cudaFree(d_plan);
   cudaFree(d_slots);
   cudaFree(d_ids);
