@@ -343,17 +343,34 @@ class Step:
         self.__dict__.update(kw)
 
 
-def make_step(gt, pool, inp, dev, stream) -> Step:
+def virtual_tables(g: synth.GatherBatch, num_pages: int, seed: int = 77):
+    """The same block tables as virtual pages: a random bijection v2p of pages
+    1..P-1 (page 0, the sink, maps to itself) and, per entry, the virtual
+    page that v2p maps to the table's physical page. Returns (virt, v2p)."""
+    rng = np.random.default_rng(seed)
+    v2p = np.zeros(num_pages, np.int32)
+    v2p[1:] = 1 + rng.permutation(num_pages - 1)
+    inv = np.zeros(num_pages, np.int32)
+    inv[v2p] = np.arange(num_pages, dtype=np.int32)
+    virt = np.where(g.block_table < 0, -1, inv[np.maximum(g.block_table, 0)]).astype(np.int32)
+    return virt, v2p
+
+
+def make_step(gt, pool, inp, dev, stream, kernel_facing: bool = False) -> Step:
     """Device buffers of one rank's inputs and the step that bench.py times:
     translate -> all-layer store of the chunk -> gather plan -> 32 x (decode
     store + planned gather) -> move, every call on `stream`. The move's ids
     are kernel-facing, translated once here with the library. The gather
     output buffers are shared by the layers (the last layer's rows remain).
-    Step.step(x, record, out) runs one step on the inputs x (Step.dev_in, or
-    any dict of device tensors of the same shapes), gathering into `out`
-    (a (K, V) pair of device tensors shaped like Step.out_k, default
-    Step.out_k / Step.out_v); with record=True it appends CUDA events around
-    each gather to Step.gather_ev."""
+    With kernel_facing the tables arrive as virtual pages with a page map:
+    the step first builds the prefix-only kernel-facing table
+    (kv_translate_block_table), then plans and gathers through it
+    (kv_gather_plan_kf, kv_gather_layer_planned_kf); the rows read are the
+    same. Step.step(x, record, out) runs one step on the inputs x
+    (Step.dev_in, or any dict of device tensors of the same shapes),
+    gathering into `out` (a (K, V) pair of device tensors shaped like
+    Step.out_k, default Step.out_k / Step.out_v); with record=True it
+    appends CUDA events around each gather to Step.gather_ev."""
     import torch
 
     L, R = SHAPE.layer_num, SHAPE.row_bytes
@@ -365,6 +382,11 @@ def make_step(gt, pool, inp, dev, stream) -> Step:
     dev_in = dict(slots=d(inp["slots"]), bt=d(g.block_table), ln=d(g.seq_len), cu=d(g.cu),
                   k_dec=d(inp["k_dec"]), v_dec=d(inp["v_dec"]), k_chunk=d(inp["k_chunk"]),
                   v_chunk=d(inp["v_chunk"]))
+    kf = None
+    if kernel_facing:
+        virt, v2p = virtual_tables(g, SHAPE.num_pages)
+        dev_in.update(virt=d(virt), v2p=d(v2p))
+        kf = torch.empty_like(dev_in["bt"])
     ids = torch.empty(N_DECODE + N_CHUNK, dtype=torch.int32, device=dev)
     mv = torch.empty(2 * N_MOVE, dtype=torch.int32, device=dev)
     gt.kv_translate(pool, d(np.concatenate([inp["move_src"], inp["move_dst"]])), mv, stream=stream)
@@ -378,21 +400,28 @@ def make_step(gt, pool, inp, dev, stream) -> Step:
         ok, ov = (out_k, out_v) if out is None else out
         gt.kv_translate(pool, x["slots"], ids, stream=stream)
         gt.kv_store_all_layers(pool, ids[N_DECODE:], x["k_chunk"], x["v_chunk"], stream=stream)
-        gt.kv_gather_plan(pool, x["bt"], x["ln"], plan=plan, stream=stream)
+        if kernel_facing:
+            gt.kv_translate_block_table(pool, x["virt"], x["ln"], x["v2p"], kf, stream=stream)
+            gt.kv_gather_plan_kf(pool, kf, x["ln"], plan=plan, stream=stream)
+        else:
+            gt.kv_gather_plan(pool, x["bt"], x["ln"], plan=plan, stream=stream)
         for layer in range(L):
             gt.kv_store_layer(pool, layer, ids[:N_DECODE], x["k_dec"][layer], x["v_dec"][layer], stream=stream)
             if record:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-            gt.kv_gather_layer_planned(pool, layer, plan, x["bt"], x["ln"], x["cu"], ok, ov, stream=stream)
+            if kernel_facing:
+                gt.kv_gather_layer_planned_kf(pool, layer, plan, kf, x["ln"], x["cu"], ok, ov, stream=stream)
+            else:
+                gt.kv_gather_layer_planned(pool, layer, plan, x["bt"], x["ln"], x["cu"], ok, ov, stream=stream)
             if record:
                 e1.record(stream)
                 gather_ev.append((e0, e1))
         gt.kv_move(pool, mv_src, mv_dst, stream=stream)
 
     return Step(step=step, dev_in=dev_in, ids=ids, mv_src=mv_src, mv_dst=mv_dst, out_k=out_k, out_v=out_v,
-                plan=plan, gather_ev=gather_ev)
+                plan=plan, gather_ev=gather_ev, kf=kf)
 
 
 
@@ -572,11 +601,33 @@ def run_gpu(args):
     # the pipelined loop's last result is the last layer's gather of its last step
     result_ok = bool(torch.equal(out_k_host[:4096].to(dev), outs[(e2e_steps - 1) % 2][0][:4096]))
 
+    # the same step with the read path of the pages: virtual tables and a page
+    # map, the prefix-only kernel-facing table built every step, the plan and
+    # the gathers reading through it (one more launch per step)
+    stk = make_step(gt, pool, inp, dev, stream, kernel_facing=True)
+    for _ in range(args.warmup):
+        stk.step(stk.dev_in)
+    barrier()
+    t0k = torch.cuda.Event(enable_timing=True)
+    t1k = torch.cuda.Event(enable_timing=True)
+    t0k.record(stream)
+    for _ in range(args.steps):
+        stk.step(stk.dev_in, record=True)
+    t1k.record(stream)
+    barrier()
+    kf_ms = t0k.elapsed_time(t1k) / args.steps
+    kf_gather_ms = statistics.mean(a.elapsed_time(b) for a, b in stk.gather_ev)
+    kf_ok = bool(torch.equal(stk.out_k, st.out_k) and torch.equal(stk.out_v, st.out_v))
+    bad |= gt.kv_pool_last_error(pool, stream)
+    del stk
+
     sb, gb = step_bytes(g)
     step_total = sum(sb.values())
+    kf_extra = g.block_table.size * (4 + 4 + 4)  # table build: virtual entry + page map entry read, entry written
     per_reader_total = step_total - sb["gather"] + L * gb["per_reader"]
-    ms, e2e_ms, e2e_ser_ms, e2e_nr_ms, gather_ms = reduce_max(
-        [ms, e2e_s["pipelined"] * 1e3, e2e_s["serial"] * 1e3, e2e_s["no_result"] * 1e3, gather_ms], dev)
+    ms, e2e_ms, e2e_ser_ms, e2e_nr_ms, gather_ms, kf_ms, kf_gather_ms = reduce_max(
+        [ms, e2e_s["pipelined"] * 1e3, e2e_s["serial"] * 1e3, e2e_s["no_result"] * 1e3, gather_ms, kf_ms,
+         kf_gather_ms], dev)
     del stages, outs, ids_sets, host, out_k_host, out_v_host
     if rank != 0:
         if world > 1:
@@ -628,6 +679,13 @@ def run_gpu(args):
                            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ser_ms, 3)},
                 "without_result_readback": {"value": round(whole_job_gbps(step_total, world, e2e_nr_ms), 1),
                                             "d2h_bytes_per_step": d2h_small, "ms_per_step": round(e2e_nr_ms, 3)}},
+        "kernel_facing_read_path": {
+            "what": "the same step with virtual block tables and a page map: kv_translate_block_table every "
+                    "step, then kv_gather_plan_kf and kv_gather_layer_planned_kf",
+            "value": round(whole_job_gbps(step_total + kf_extra, world, kf_ms), 1), "unit": "GB/s",
+            "ms_per_step": round(kf_ms, 4), "gather_avg_launch_ms": round(kf_gather_ms, 4),
+            "gather_frac": round(gb["method"] / (kf_gather_ms * 1e-3) / GB / measured_hbm_peak()[0], 4),
+            "output_equals_physical_table_step": kf_ok, "steps": args.steps},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "device_errors": dev_err | bad,
