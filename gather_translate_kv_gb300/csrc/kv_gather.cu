@@ -36,12 +36,20 @@ namespace {
 #endif
 // Latent rows of 1152 bytes (the 576-element bf16 latent of DeepSeek-like
 // MLA pools, 72 vectors) fit 7 to a round of 32 x 16 vectors, so a 64-row
-// page takes 10 rounds, the last one for a single row; rounds of 32 x 18
-// vectors hold exactly 8 such rows. Measured on the 128 x 4096-token MLA
-// gather: table order 184 -> 176 us, but the planned gather 152 -> 164 us
-// (its 18-vector instance spills), so only the table-order gather uses them.
+// page takes 10 rounds, the last one for a single row. Rounds whose vectors
+// hold whole rows do better, measured on the 128 x 4096-token MLA gather:
+// in table order rounds of 32 x 18 vectors (8 rows) take it from 184 to
+// 176 us; the planned gather is best with rounds of 32 x 9 vectors (4 rows,
+// 80 registers: 3 blocks per SM), 154 -> 144 us (18-vector rounds spill
+// there and were slower, 164 us).
 #ifndef GTKV_GATHER_V72
 #define GTKV_GATHER_V72 1
+#endif
+#ifndef GTKV_GATHER_V72_TABLE_CHV
+#define GTKV_GATHER_V72_TABLE_CHV 18  // vectors per lane per round, table order (a multiple of 9)
+#endif
+#ifndef GTKV_GATHER_V72_PLANNED_CHV
+#define GTKV_GATHER_V72_PLANNED_CHV 9  // vectors per lane per round, page-major plan (a multiple of 9)
 #endif
 // Blocks per SM the register allocation must allow (0: left to the compiler,
 // which keeps these kernels at 2 blocks of 256 threads per SM; 3 or 4 blocks
@@ -273,18 +281,19 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
   int64_t cpp = (p.ps + chunk_rows - 1) / chunk_rows;
   // one round: 32 lanes x 8 vectors = 4 KiB of K and 4 KiB of V (latent: 8 KiB of K) in flight per warp
   constexpr int CHV = GTKV_GATHER_CHV;
-  const int kind = !latent ? 0 : (GTKV_GATHER_V72 && p.vpr == 72 && plan == nullptr ? 2 : 1);
+  const int kind = !latent ? 0 : (GTKV_GATHER_V72 && p.vpr == 72 ? 2 : 1);
+  constexpr int V72T = GTKV_GATHER_V72_TABLE_CHV, V72P = GTKV_GATHER_V72_PLANNED_CHV;
   using Kernel = decltype(&k_gather_runs<CHV, true, true, false>);
   const Kernel kernels[3][2][2] = {  // [MHA / latent / 1152-byte latent][plan][kernel_facing]
       {{k_gather_runs<CHV, false, true, false>, k_gather_runs<CHV, false, true, true>},
        {k_gather_runs<CHV, true, true, false>, k_gather_runs<CHV, true, true, true>}},
       {{k_gather_runs<2 * CHV, false, false, false>, k_gather_runs<2 * CHV, false, false, true>},
        {k_gather_runs<2 * CHV, true, false, false>, k_gather_runs<2 * CHV, true, false, true>}},
-      {{k_gather_runs<18, false, false, false>, k_gather_runs<18, false, false, true>},
-       {nullptr, nullptr}}};
+      {{k_gather_runs<V72T, false, false, false>, k_gather_runs<V72T, false, false, true>},
+       {k_gather_runs<V72P, true, false, false>, k_gather_runs<V72P, true, false, true>}}};
   const Kernel kernel = kernels[kind][plan != nullptr][kernel_facing];
   if (latent) {
-    chunk_rows = rows_per_item(kind == 2 ? 32 * 18 * 16 : 2 * GTKV_GATHER_CHUNK);
+    chunk_rows = rows_per_item(kind == 2 ? 32 * 16 * (plan != nullptr ? V72P : V72T) : 2 * GTKV_GATHER_CHUNK);
     cpp = (p.ps + chunk_rows - 1) / chunk_rows;
   }
   int64_t warps = static_cast<int64_t>(n_seqs) * max_pages * cpp;
