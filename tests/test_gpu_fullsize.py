@@ -302,27 +302,34 @@ def test_id_bound_stress_full():
     F.close()
 
 
-def test_bench_step_full():
+@pytest.mark.parametrize("kernel_facing", [False, True], ids=["physical_tables", "kernel_facing_tables"])
+def test_bench_step_full(kernel_facing):
     """The step bench.py times, on its own inputs and in its own launch
     configuration (bench.make_step on the full 8 GiB decode pool), run twice
-    as its warm-up does. Then the oracle's address mode checks every row the
-    step wrote or read: the 512 translated ids, the 256-token chunk and the
-    256 decode tokens in all 32 layers, every row of the last layer's planned
-    gather (256 x 4096 tokens; it reads rows the stores and the previous
-    step's move wrote), the 64 row-blocks of the 8192 moved tokens, and that
-    no other row of the pool changed."""
+    as its warm-up does; also in its kernel-facing form (virtual tables and
+    a page map, the table built every step, plan and gathers through it).
+    Then the oracle's address mode checks every row the step wrote or read:
+    the 512 translated ids, the 256-token chunk and the 256 decode tokens in
+    all 32 layers, every row of the last layer's planned gather (256 x 4096
+    tokens; it reads rows the stores and the previous step's move wrote), the
+    64 row-blocks of the 8192 moved tokens, and that no other row of the pool
+    changed."""
     import bench
 
     sh = bench.SHAPE
     F = Full(sh)
     inp = bench.make_inputs(0)
     st = bench.make_step(gt, F.pool, inp, torch.device("cuda", torch.cuda.current_device()),
-                         torch.cuda.current_stream())
+                         torch.cuda.current_stream(), kernel_facing=kernel_facing)
     for _ in range(2):
         st.step(st.dev_in)
     torch.cuda.synchronize()
     assert gt.kv_pool_last_error(F.pool) == 0
     L, R = sh.layer_num, F.R
+    if kernel_facing:
+        virt, v2p = bench.virtual_tables(inp["g"], sh.num_pages)
+        kf_ref, err = F.o.block_table_kf(virt, inp["g"].seq_len, v2p, out=np.zeros_like(virt))
+        assert err == 0 and np.array_equal(st.kf.cpu().numpy(), kf_ref), "kernel-facing table differs"
 
     slots = inp["slots"]
     ids_ref, err = F.o.translate(slots)
@@ -355,7 +362,10 @@ def test_bench_step_full():
     # the gather buffers hold the last layer's rows; the second step's gather
     # ran after the first step's move
     g = inp["g"]
-    ks, vs, err = F.o.gather_rows(L - 1, g.block_table, g.seq_len, g.cu, g.seq_start)
+    if kernel_facing:
+        ks, vs, err = F.o.gather_rows(L - 1, kf_ref, g.seq_len, g.cu, g.seq_start, kernel_facing=True)
+    else:
+        ks, vs, err = F.o.gather_rows(L - 1, g.block_table, g.seq_len, g.cu, g.seq_start)
     assert err == 0 and (ks >= 0).all() and (vs >= 0).all()
     assert torch.equal(st.out_k, F.expected_reads(ks, last_k + [(db, moved)])), "gathered K differs"
     assert torch.equal(st.out_v, F.expected_reads(vs, last_v + [(db, moved)])), "gathered V differs"
