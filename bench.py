@@ -447,7 +447,8 @@ def run_targets(iters: int) -> dict:
         key = f"{key}:{rec['cfg']}"
         out[key] = {"what": TARGET_NAMES[key], "us_per_call": rec["us_per_call"],
                     "method_bytes_per_call": rec["useful_bytes_per_call"], "GBps": rec["useful_GBps"],
-                    "frac": round(rec["pct_of_hbm_peak"] / 100, 4), "calls": rec["calls"],
+                    "frac": round(rec["pct_of_hbm_peak"] / 100, 4), "rows_per_s": rec["rows_per_s"],
+                    "calls": rec["calls"],
                     "l2_flush": rec.get("l2_flush")}
     return out
 
@@ -624,6 +625,7 @@ def run_gpu(args):
     sb, gb = step_bytes(g)
     step_total = sum(sb.values())
     kf_extra = g.block_table.size * (4 + 4 + 4)  # table build: virtual entry + page map entry read, entry written
+    step_rows = (L * gb["rows"] * 2 + N_CHUNK * 2 * L + L * N_DECODE * 2 + N_MOVE * 2 * L)  # K and V rows
     per_reader_total = step_total - sb["gather"] + L * gb["per_reader"]
     ms, e2e_ms, e2e_ser_ms, e2e_nr_ms, gather_ms, kf_ms, kf_gather_ms = reduce_max(
         [ms, e2e_s["pipelined"] * 1e3, e2e_s["serial"] * 1e3, e2e_s["no_result"] * 1e3, gather_ms, kf_ms,
@@ -657,6 +659,8 @@ def run_gpu(args):
                    "l2": "no flush: inputs larger than L2 (8 GiB pool, 4 GiB gather output per layer)",
                    "parallelism": f"replicas x{world}",
                    "pct_of_hbm_peak": round(100 * step_total / (ms * 1e-3) / GB / peak, 1),
+                   # rows copied per second: the gathers' output rows, the stores' and the move's rows
+                   "rows_per_s": round(world * step_rows / (ms * 1e-3), 1),
                    # every output row's source counted once per sequence that reads it; L2 serves the
                    # repeats, so this rate is not bounded by the HBM peak
                    "effective_GBps_per_reader": round(whole_job_gbps(per_reader_total, world, ms), 1),
