@@ -336,11 +336,11 @@ int kv_gather_layer_planned(const kv_pool_t* pool, int32_t layer, const void* pl
  * Set-up: the first call on each device looks up the array's device address
  * with that device current (cudaGetSymbolAddress), and so does the first
  * call after the device's context was created anew (cudaDeviceReset); make
- * that first call before any stream capture. Sharing: every call uses the same array, which
- * keeps the previous call's contents; each call clears the counters it uses
- * on its stream first, so calls ordered on the GPU are independent, but calls
- * that overlap on the GPU (different streams, threads or pools on one device)
- * race on the array and give wrong plans: order them. */
+ * that first call before any stream capture. Sharing: every call uses the
+ * same array, which keeps the previous call's contents; each call clears the
+ * counters it uses on its stream first, so calls ordered on the GPU are
+ * independent, but calls that overlap on the GPU (different streams, threads
+ * or pools on one device) race on the array and give wrong plans: order them. */
 int kv_gather_plan_noalloc(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs,
                            int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
                            void* plan_dev, int64_t plan_bytes, kv_stream_t stream);
