@@ -753,7 +753,7 @@ MICRO_DEFAULT = ["ceiling:0", "translate:2", "block_table:2", "store:2", "store_
                  "gather:2", "gather_planned:2", "move:2",
                  "translate:3", "store:3", "store_slots:3", "store_all:3", "gather:3", "gather_planned:3",
                  "translate_mapped:4", "store:4", "gather:4", "gather_planned:4", "move:4",
-                 "translate:5", "store:5", "store_slots:5", "gather:5", "gather_planned:5", "move:5",
+                 "translate:5", "store:5", "store_sorted:5", "store_slots:5", "gather:5", "gather_planned:5", "move:5", "move_sorted:5",
                  "store:6", "store_all:6", "gather:6", "gather_planned:6", "move:6"]
 
 
@@ -923,7 +923,7 @@ def run_micro(args, quiet: bool = False) -> list[dict]:
             ms = timed(lambda i: gt.kv_translate_block_table(pool, vt, lnt, vmap, kf), calls, True)
             report("translate_block_table", cfg, f"{gbt.block_table.shape[0]} x {gbt.block_table.shape[1]} entries",
                    ms, ne * 12, ne)
-        if "store" in kernels or "store_graph" in kernels or "store_slots" in kernels:
+        if "store" in kernels or "store_graph" in kernels or "store_slots" in kernels or "store_sorted" in kernels:
             K = _payload_torch(gen, n, R, sh.itemsize, dev)
             V = None if sh.latent else _payload_torch(gen, n, R, sh.itemsize, dev)
             useful = (n - n_tomb) * 2 * kvr * R + n * 4
@@ -939,6 +939,17 @@ def run_micro(args, quiet: bool = False) -> list[dict]:
                 ref = timed(ref_store, max(calls, L), flush) if args.torch_ref else None
                 report("store_layer", cfg, f"{n} tokens per layer ({n_tomb} tombstones)", ms, useful, 2 * n,
                        {"l2_flush": flush, "tombstone_bytes": n_tomb * 4 * R}, ref)
+            if "store_sorted" in kernels:
+                # the same tokens in destination order, their K/V rows permuted alike (done here,
+                # outside the timing): how much of the store's time is where its rows land
+                order = torch.argsort(ids)
+                ids_s = ids[order].contiguous()
+                K_s = K[order].contiguous()
+                V_s = None if V is None else V[order].contiguous()
+                ms = timed(lambda i: gt.kv_store_layer(pool, i % L, ids_s, K_s, V_s), max(calls, L), flush)
+                report("store_layer_sorted", cfg, f"{n} tokens per layer in destination order ({n_tomb} tombstones)",
+                       ms, useful, 2 * n, {"l2_flush": flush})
+                del ids_s, K_s, V_s
             if "store_slots" in kernels:
                 ms = timed(lambda i: gt.kv_store_layer_slots(pool, i % L, slots_d, K, V), max(calls, L), flush)
                 report("store_layer_slots", cfg, f"{n} slots per layer, translate fused ({n_tomb} tombstones)",
@@ -1018,24 +1029,32 @@ def run_micro(args, quiet: bool = False) -> list[dict]:
                 report("gather_layer", cfg, f"{gb.block_table.shape[0]} seqs, {rows} rows", ms, useful, rows, share,
                        ref)
             del ok, ov
-        if "move" in kernels:
+        if "move" in kernels or "move_sorted" in kernels:
             src, dst = synth.move_slots(sh)
             m = src.size
             mv = torch.empty(2 * m, dtype=torch.int32, device=dev)
             gt.kv_translate(pool, d(np.concatenate([src, dst])), mv)
             useful = m * (kvr * L * R * 2 + 8)
             flush = useful < 4 * l2
-            ms = timed(lambda i: gt.kv_move(pool, mv[:m], mv[m:]), calls, flush)
-            ref = None
-            if args.torch_ref:
-                s64, d64 = mv[:m].to(torch.int64), mv[m:].to(torch.int64)
+            if "move_sorted" in kernels:  # the same pairs in destination order (sorted outside the timing)
+                order = torch.argsort(mv[m:])
+                ms_s, md_s = mv[:m][order].contiguous(), mv[m:][order].contiguous()
+                ms = timed(lambda i: gt.kv_move(pool, ms_s, md_s), calls, flush)
+                report("move_sorted", cfg, f"{m} tokens x {kvr * L} row-blocks in destination order", ms, useful,
+                       kvr * L * m, {"l2_flush": flush})
+            if "move" in kernels:
+                ms = timed(lambda i: gt.kv_move(pool, mv[:m], mv[m:]), calls, flush)
+                ref = None
+                if args.torch_ref:
+                    s64, d64 = mv[:m].to(torch.int64), mv[m:].to(torch.int64)
 
-                def ref_move(i):  # every layer's K and V view, one indexing op each
-                    for b in range(kvr * L):
-                        vb = view(b)
-                        vb[d64] = vb[s64]
-                ref = timed(ref_move, max(3, calls // 4), flush)
-            report("move", cfg, f"{m} tokens x {kvr * L} row-blocks", ms, useful, kvr * L * m, {"l2_flush": flush}, ref)
+                    def ref_move(i):  # every layer's K and V view, one indexing op each
+                        for b in range(kvr * L):
+                            vb = view(b)
+                            vb[d64] = vb[s64]
+                    ref = timed(ref_move, max(3, calls // 4), flush)
+                report("move", cfg, f"{m} tokens x {kvr * L} row-blocks", ms, useful, kvr * L * m,
+                       {"l2_flush": flush}, ref)
         err = gt.kv_pool_last_error(pool)
         assert err == 0, f"device error bits {err}"
         gt.kv_pool_destroy(pool)
