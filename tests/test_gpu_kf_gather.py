@@ -158,6 +158,27 @@ def test_kf_gather_matches_oracle(shape, anchor, latent):
             assert_bytes_equal(dk, ok, f"kf gather K ({how}) layer {layer}", R)
             if not latent:
                 assert_bytes_equal(dv, ov, f"kf gather V ({how}) layer {layer}", R)
+    # in place: past each sequence's prefix the table keeps its virtual pages
+    # (off the 2L grid unless 2L divides them); the gathers never read there,
+    # so they raise no bit and give the same rows
+    ip_d = to_dev(virt.copy())
+    gt.kv_translate_block_table(pp.pool, ip_d, to_dev(ln), to_dev(v2p))
+    assert pp.last_error() == 0
+    ip = ip_d.cpu().numpy()
+    pre = np.arange(maxp)[None, :] < -(-ln[:, None] // ps)
+    assert np.array_equal(ip[pre], kf_ref[pre]) and np.array_equal(ip[~pre], virt[~pre])
+    plan_ip = gt.kv_gather_plan_kf(pp.pool, ip_d, to_dev(ln), to_dev(st))
+    assert pp.last_error() == 0
+    rows = g.total + 3
+    ok = np.full((rows, R), 0x5A, np.uint8)
+    ov = None if latent else np.full((rows, R), 0x5A, np.uint8)
+    ok, ov, err = o.gather_kf(pp.M, L - 1, kf_ref, ln, g.cu, st, rows, ok, ov)
+    for how, (dk, dv) in zip(("table", "planned"), _gpu_gathers(pp, L - 1, ip_d, ln, g.cu, st, rows, latent,
+                                                               plan_ip)):
+        assert pp.last_error() == 0
+        assert_bytes_equal(dk, ok, f"kf gather K over an in-place table ({how})", R)
+        if not latent:
+            assert_bytes_equal(dv, ov, f"kf gather V over an in-place table ({how})", R)
     pp.close()
 
 
