@@ -665,7 +665,7 @@ def run_gpu(args):
                    # repeats, so this rate is not bounded by the HBM peak
                    "effective_GBps_per_reader": round(whole_job_gbps(per_reader_total, world, ms), 1),
                    "useful_bytes_per_output_reference": per_reader_total},
-        "roofline": {"bound": "hbm", "kernel": "kv_gather_layer_planned (k_gather_runs<8, true, true>)",
+        "roofline": {"bound": "hbm", "kernel": "kv_gather_layer_planned (k_gather_fan<true, false>)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": gb["method"],

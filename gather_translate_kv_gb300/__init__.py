@@ -29,7 +29,7 @@ STATUS = {
     -4: "KV_ERR_TAIL_PAD", -5: "KV_ERR_ALIGN", -6: "KV_ERR_CUDA", -7: "KV_ERR_DEVICE",
     -8: "KV_ERR_CAPACITY",
 }
-KV_DEV_ERR_ROW, KV_DEV_ERR_V2P, KV_DEV_ERR_TABLE, KV_DEV_ERR_FORM = 1, 2, 4, 8
+KV_DEV_ERR_ROW, KV_DEV_ERR_V2P, KV_DEV_ERR_TABLE, KV_DEV_ERR_FORM, KV_DEV_ERR_TIMEOUT = 1, 2, 4, 8, 16
 
 
 class KVError(RuntimeError):
@@ -99,7 +99,14 @@ def lib():
             f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
             "(there is no fallback implementation)"
         )
-    L = ctypes.CDLL(LIB_PATH)
+    _lib = load(LIB_PATH)
+    return _lib
+
+
+def load(path: str) -> ctypes.CDLL:
+    """A library built from these sources (libgtkv.so, or a build with other
+    flags), with the argument types of include/kv_pool.h set."""
+    L = ctypes.CDLL(path)
     P, vp, i32, i64 = ctypes.POINTER, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     sig = {
         "kv_pool_required_bytes": [P(kv_pool_desc), P(i64), P(i64)],
@@ -130,7 +137,6 @@ def lib():
         f.restype = ctypes.c_int
     L.kv_status_string.argtypes = [ctypes.c_int]
     L.kv_status_string.restype = ctypes.c_char_p
-    _lib = L
     return L
 
 

@@ -18,6 +18,10 @@
 // vectors, all loads of a round issued before its stores. No
 // search and no host synchronization: the item space is n_seqs x max_pages x
 // chunks_per_page, and an entry outside a sequence's window is an empty item.
+//
+// A planned gather over a table of at least num_pages entries takes the
+// fan-out form instead (k_gather_fan, below): each page is staged once in
+// shared memory and bulk-copied to all of its readers.
 #include "kv_launch.h"
 #include "kv_plan.cuh"
 
@@ -261,6 +265,218 @@ __global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const
   }
 }
 
+// ---- fan-out form of the planned gather ----------------------------------
+//
+// With a page-major plan the readers of a page are consecutive plan
+// positions. A block of one warp takes `group` consecutive positions (whole
+// table entries), loads the rows of each page they name into shared memory
+// once (bulk copy, completion counted on an mbarrier) and writes them to every
+// reader's output rows with bulk stores: a page shared by n readers is read
+// from L2 n / group times instead of n times, and the output leaves through
+// the bulk-copy engine in whole-entry runs. The grid is not persistent (one
+// block per `group` positions, balanced over the SMs by the hardware block
+// scheduler): on this GPU a persistent grid writes at ~6.5 TB/s whatever its
+// store form, short blocks at ~7.5 TB/s. A block whose positions name several
+// pages keeps up to `nbuf` page loads in flight (one buffer and one mbarrier
+// each), issued in the order the pages are written.
+//
+// Measured on the decode gather (256 x 4096 tokens over tables that name every
+// page ~16 times): 742 -> 708 us against the vector kernel's page-major walk;
+// 2 positions per block is as fast as 3 or 4 there and the best on the MLA
+// gather (142 -> 131 us). Where pages are read once a block of two entries
+// ends with the later of two loads, which cost the SWA gather 5 %; so the
+// launcher takes this form only for tables with at least as many entries as
+// the pool has pages, where the page-major walk is the one that pays.
+
+#ifndef GTKV_GATHER_FANOUT
+#define GTKV_GATHER_FANOUT 1  // 0: planned gathers always take the vector kernel
+#endif
+#ifndef GTKV_FAN_GROUP
+#define GTKV_FAN_GROUP 2  // plan positions per block (1..32)
+#endif
+#ifndef GTKV_FAN_MAX_BYTES
+#define GTKV_FAN_MAX_BYTES 73728  // shared memory per block for page buffers (a 64-row 1152-byte latent page)
+#endif
+// Bytes the load barrier expects beyond what the loads deliver: 0, except in
+// the test build that checks the bounded wait (its loads never "land").
+#ifndef GTKV_FAN_TEST_EXTRA_TX
+#define GTKV_FAN_TEST_EXTRA_TX 0
+#endif
+
+static_assert(GTKV_FAN_GROUP >= 1 && GTKV_FAN_GROUP <= 32, "one warp per block");
+constexpr uint32_t kFanSpinLimit = 1u << 24;  // barrier polls before a load is given up on (~1 s)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Polls the barrier's phase `parity` at most kFanSpinLimit times.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kFanSpinLimit; ++i)
+    if (mbar_test(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                          uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes), "l"(pol)
+               : "memory");
+}
+
+template <bool HAS_V, bool KF>
+__global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, const int32_t* __restrict__ bt,
+                                                   int32_t n_seqs, int32_t max_pages,
+                                                   const int32_t* __restrict__ seq_start,
+                                                   const int32_t* __restrict__ seq_len,
+                                                   const int64_t* __restrict__ cu, uint4* __restrict__ out_k,
+                                                   uint4* __restrict__ out_v, int64_t out_rows,
+                                                   const int32_t* __restrict__ plan, int group, int nbuf) {
+  extern __shared__ __align__(128) uint4 sbuf[];  // nbuf buffers: a page's K rows of the layer, then its V rows
+  __shared__ __align__(8) uint64_t bars[32];
+  const int lane = threadIdx.x;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  check_gather_meta(p, n_seqs, max_pages, seq_start, seq_len, cu, out_rows, tid,
+                    static_cast<int64_t>(gridDim.x) * 32);
+  const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
+  const int32_t flags = __ldg(plan + 3);
+  if (__ldg(plan + 1) != n_seqs || __ldg(plan + 2) != max_pages || ((flags & kPlanKernelFacing) != 0) != KF) {
+    if (tid == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
+    return;
+  }
+  int64_t n_units = n_entries;
+  const int32_t* order = nullptr;
+  if (flags & kPlanPageMajor) {
+    const int64_t np = __ldg(plan);
+    n_units = np < 0 ? 0 : (np > n_entries ? n_entries : np);
+    order = plan + kPlanHeaderWords + p.num_pages + 1;
+  }
+  const int64_t vpr = p.vpr;
+  const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * p.ps;
+  const L2Policy pol = make_l2_policy();
+
+  // lane j < group: plan position blockIdx.x * group + j, a whole table entry
+  Run mine{0, 0, 0, 0};
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * group + lane;
+  if (lane < group && u < n_units) {
+    int64_t sk = u;
+    bool ok = true;
+    if (order != nullptr) {
+      sk = __ldg(order + u);
+      if (sk < 0 || sk >= n_entries) {
+        atomicOr(p.err, KV_DEV_ERR_TABLE);
+        ok = false;
+      }
+    }
+    if (ok)
+      mine = gather_item<KF>(p, sk, 0, koff, bt, max_pages, seq_start, seq_len, cu, out_rows,
+                             static_cast<int32_t>(p.ps), true);
+  }
+  // a page run: page pg, rows [off, off + nrows) of the layer's block
+  int64_t pg = -1;
+  int32_t off = 0, nrows = 0;
+  if (mine.kind == 1) {
+    const int64_t r = mine.src / vpr;
+    pg = r / p.stride;
+    off = static_cast<int32_t>(r - pg * p.stride - koff);
+    nrows = static_cast<int32_t>(mine.nvec / vpr);
+  }
+
+  // Page groups: the block's runs that name one page, numbered in the order
+  // of their lowest lane; group g's rows [lo, hi) of the page go to buffer
+  // g % nbuf, and its lowest lane issues that load.
+  int my_g = -1, lead_g = -1, ng = 0;
+  int32_t g_lo = 0, g_hi = 0;
+  int64_t g_pg = 0;
+  for (unsigned t = __ballot_sync(kFull, mine.kind == 1); t; ++ng) {
+    const int lead = __ffs(t) - 1;
+    const int64_t gp = __shfl_sync(kFull, pg, lead);
+    const bool in = mine.kind == 1 && pg == gp;
+    const unsigned members = __ballot_sync(kFull, in);
+    const int32_t lo = __reduce_min_sync(kFull, in ? off : INT32_MAX);
+    const int32_t hi = __reduce_max_sync(kFull, in ? off + nrows : 0);
+    if (in) my_g = ng;
+    if (lane == lead) {
+      lead_g = ng;
+      g_lo = lo;
+      g_hi = hi;
+      g_pg = gp;
+    }
+    t &= ~members;
+  }
+  if (ng > 0) {
+    const int64_t buf_vecs = p.kv_rows * p.ps * vpr;
+    if (lane < nbuf) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + lane)) : "memory");
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    auto issue = [&](int b) {  // by the lane that leads the group
+      const uint32_t bytes = static_cast<uint32_t>((g_hi - g_lo) * vpr * 16);
+      uint4* sb = sbuf + b * buf_vecs;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bars + b)),
+                   "r"((HAS_V ? 2 * bytes : bytes) + GTKV_FAN_TEST_EXTRA_TX)
+                   : "memory");
+      const uint4* src = p.base + (g_pg * p.stride + koff + g_lo) * vpr;
+      bulk_load(sb + g_lo * vpr, src, bytes, bars + b, pol.keep);
+      if (HAS_V) bulk_load(sb + (p.ps + g_lo) * vpr, src + p.ps * vpr, bytes, bars + b, pol.keep);
+    };
+    if (lead_g >= 0 && lead_g < nbuf) issue(lead_g);
+    for (int g = 0; g < ng; ++g) {
+      const int b = g % nbuf;
+      if (!__all_sync(kFull, mbar_wait_bounded(bars + b, (g / nbuf) & 1))) {
+        // a load that never landed: flag it, give the loads in flight one more
+        // bounded wait, then leave
+        if (lane == 0) atomicOr(p.err, KV_DEV_ERR_TIMEOUT);
+        for (int q = g; q < ng && q < g + nbuf; ++q) mbar_wait_bounded(bars + q % nbuf, (q / nbuf) & 1);
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        return;
+      }
+      if (my_g == g) {
+        const uint32_t run = static_cast<uint32_t>(nrows * vpr * 16);
+        const uint4* sb = sbuf + b * buf_vecs;
+        bulk_store(out_k + mine.row * vpr, sb + off * vpr, run, pol.first);
+        if (HAS_V) bulk_store(out_v + mine.row * vpr, sb + (p.ps + off) * vpr, run, pol.first);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+      if (g + nbuf < ng) {  // group g + nbuf reuses buffer b: group g's stores must have read it
+        if (my_g == g) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        if (lead_g == g + nbuf) issue(b);
+      }
+    }
+  }
+  // tombstoned entries: every token of the run reads the page-0 sink row
+  const unsigned sinks = __ballot_sync(kFull, mine.kind == 2);
+  for (unsigned m = sinks; m; m &= m - 1) {
+    const int j = __ffs(m) - 1;
+    const int64_t row = __shfl_sync(kFull, mine.row, j);
+    const int64_t nvec = __shfl_sync(kFull, mine.nvec, j);
+    const uint4* srck = p.base + __shfl_sync(kFull, mine.src, j);
+    for (int64_t v = lane; v < nvec; v += 32) {
+      const int64_t col = v % vpr;
+      st16<GTKV_GATHER_ST>(out_k + row * vpr + v, ld16<GTKV_GATHER_LD>(srck + col, pol), pol);
+      if (HAS_V)
+        st16<GTKV_GATHER_ST>(out_v + row * vpr + v, ld16<GTKV_GATHER_LD>(srck + p.ps * vpr + col, pol), pol);
+    }
+  }
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // shared memory must outlive the stores' reads
+}
+
 }  // namespace
 
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
@@ -271,6 +487,32 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
   // latent-only pool has no V, so its items take twice the K bytes and keep
   // the same bytes in flight per warp
   const bool latent = p.kv_rows == 1;
+  const int64_t page_layer_bytes = static_cast<int64_t>(p.kv_rows) * p.ps * p.vpr * 16;
+  const int64_t n_table = static_cast<int64_t>(n_seqs) * max_pages;
+  if (GTKV_GATHER_FANOUT && plan != nullptr && page_layer_bytes <= GTKV_FAN_MAX_BYTES && n_table >= p.num_pages) {
+    using FanKernel = decltype(&k_gather_fan<true, false>);
+    const FanKernel fans[2][2] = {{k_gather_fan<true, false>, k_gather_fan<true, true>},
+                                  {k_gather_fan<false, false>, k_gather_fan<false, true>}};
+    const FanKernel fan = fans[latent][kernel_facing];
+    constexpr int group = GTKV_FAN_GROUP;
+    // page buffers per block: as many as GTKV_FAN_MAX_BYTES holds, at most one per position
+    int64_t nbuf = GTKV_FAN_MAX_BYTES / page_layer_bytes;
+    if (nbuf > group) nbuf = group;
+    if (nbuf < 1) nbuf = 1;
+    const int smem = static_cast<int>(nbuf * page_layer_bytes);
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(fan, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+    }
+    int64_t blocks = (n_table + group - 1) / group;
+    const int64_t seq_blocks = (static_cast<int64_t>(n_seqs) + 31) / 32;  // the metadata checks
+    if (blocks < seq_blocks) blocks = seq_blocks;
+    if (blocks < 1) blocks = 1;
+    fan<<<static_cast<unsigned>(blocks), 32, smem, s>>>(p, layer, bt, n_seqs, max_pages, seq_start, seq_len, cu,
+                                                       static_cast<uint4*>(out_k), static_cast<uint4*>(out_v),
+                                                       out_rows, plan, group, static_cast<int>(nbuf));
+    return cudaGetLastError();
+  }
   auto rows_per_item = [&](int64_t bytes) {
     int64_t r = bytes / (16 * p.vpr);
     if (r < 1) r = 1;

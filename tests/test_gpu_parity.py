@@ -830,3 +830,54 @@ def test_planned_gather_matches_oracle(shape, anchor, latent):
     assert pp.last_error() == gt.KV_DEV_ERR_TABLE
     assert bool((dk == 0x33).all())
     pp.close()
+
+
+@pytest.mark.parametrize("shape,anchor,latent", [(synth.SHAPES[2].scaled(40), 0, False), (SHAPES[5][0], 16, False),
+                                                 (synth.SHAPES[5].scaled(20), 0, False),
+                                                 (MLA_SHAPES[0][0], 0, True)],
+                         ids=["R2048-ps16", "odd-rows", "R64-ps256", "mla-r1152"])
+def test_planned_gather_both_forms(shape, anchor, latent):
+    """kv_gather_layer_planned has two kernels with one output: blocks that
+    stage each page in shared memory and bulk-copy it to its readers (tables
+    of at least num_pages entries, when one page's rows of a layer fit in
+    72 KiB) and warps that copy through registers (smaller tables). The same
+    pool read through a table on each side of that rule, with shared pages,
+    tombstoned entries, windows starting mid-page and gaps between the
+    output spans, must equal the oracle's gather, in both table forms."""
+    rng = np.random.default_rng(700 + shape.row_bytes)
+    pp = PoolPair(shape, anchor, latent=latent)
+    o, R, L, ps, P = pp.o, pp.R, shape.layer_num, shape.page_size, shape.num_pages
+    B = pp.pool.info["blocks_per_page"]
+    assert (2 - latent) * ps * R <= 73728
+    maxp = min(P - 1, 6)
+    for S_ in (-(-P // maxp) + 3, max(1, (P - 1) // maxp)):  # n_seqs * max_pages >= P, then < P
+        fan = S_ * maxp >= P
+        bt = np.where(rng.random((S_, maxp)) < 0.7, rng.integers(1, min(P, 6), size=(S_, maxp)),
+                      rng.integers(1, P, size=(S_, maxp))).astype(np.int32)
+        bt[rng.random((S_, maxp)) < 0.05] = -1
+        ln = rng.integers(0, maxp * ps + 1, size=S_).astype(np.int32)
+        ln[0] = maxp * ps
+        st = np.minimum(rng.integers(0, 2 * ps, size=S_), ln).astype(np.int32)
+        cu = np.zeros(S_ + 1, np.int64)
+        cu[1:] = np.cumsum(ln - st + rng.integers(0, 3, size=S_))  # gaps between the spans stay untouched
+        rows = int(cu[-1]) + 2
+        kf = np.where(bt >= 0, bt * B, bt).astype(np.int32)
+        for form, table in (("physical", bt), ("kernel-facing", kf)):
+            plan = (gt.kv_gather_plan_kf if form == "kernel-facing" else gt.kv_gather_plan)(
+                pp.pool, to_dev(table), to_dev(ln), to_dev(st))
+            assert pp.last_error() == 0
+            for layer in sorted({0, L - 1}):
+                ok = np.full((rows, R), 0x11, np.uint8)
+                ov = None if latent else np.full((rows, R), 0x22, np.uint8)
+                ok, ov, err = o.gather(pp.M, layer, bt, ln, cu, st, rows, ok, ov)
+                assert err == 0
+                dk = torch.full((rows, R), 0x11, dtype=torch.uint8, device="cuda")
+                dv = None if latent else torch.full((rows, R), 0x22, dtype=torch.uint8, device="cuda")
+                fn = gt.kv_gather_layer_planned_kf if form == "kernel-facing" else gt.kv_gather_layer_planned
+                fn(pp.pool, layer, plan, to_dev(table), to_dev(ln), to_dev(cu), dk, dv, to_dev(st))
+                assert pp.last_error() == 0
+                what = f"{'fan-out' if fan else 'vector'} planned gather, {form} table, layer {layer}"
+                assert_bytes_equal(dk.cpu().numpy(), ok, what + " K", R)
+                if not latent:
+                    assert_bytes_equal(dv.cpu().numpy(), ov, what + " V", R)
+    pp.close()

@@ -25,6 +25,17 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"libgtkv.so does not export {n}"
 
 
+def test_device_error_bits_match_the_header():
+    """The binding's KV_DEV_ERR_* constants are the header's #defines."""
+    import re
+
+    defs = dict(re.findall(r"^#define (KV_DEV_ERR_\w+) (\d+)", open(gt.HEADER).read(), flags=re.M))
+    assert set(defs) == {"KV_DEV_ERR_ROW", "KV_DEV_ERR_V2P", "KV_DEV_ERR_TABLE", "KV_DEV_ERR_FORM",
+                         "KV_DEV_ERR_TIMEOUT"}
+    for name, value in defs.items():
+        assert getattr(gt, name) == int(value), name
+
+
 def test_status_strings(lib):
     for code, name in gt.STATUS.items():
         assert gt.kv_status_string(code) == name
