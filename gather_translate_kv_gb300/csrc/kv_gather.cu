@@ -19,9 +19,11 @@
 // search and no host synchronization: the item space is n_seqs x max_pages x
 // chunks_per_page, and an entry outside a sequence's window is an empty item.
 //
-// A planned gather over a table of at least num_pages entries takes the
-// fan-out form instead (k_gather_fan, below): each page is staged once in
-// shared memory and bulk-copied to all of its readers.
+// Where one page's rows of a layer fit in 72 KiB of shared memory, gathers take
+// the fan-out form instead (k_gather_fan, below): a block stages each page it
+// needs once in shared memory and bulk-copies it to its readers -- with a plan
+// (over tables of at least num_pages entries) all readers of a page in its
+// positions, without one a single table entry.
 #include "kv_launch.h"
 #include "kv_plan.cuh"
 
@@ -297,6 +299,16 @@ __global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const
 #ifndef GTKV_FAN_MAX_BYTES
 #define GTKV_FAN_MAX_BYTES 73728  // shared memory per block for page buffers (a 64-row 1152-byte latent page)
 #endif
+// Gathers without a plan take the same kernel in table order, one entry per
+// block (a block of one entry waits for one load only): on the decode tables,
+// whose pages are named ~16 times, 1241 -> 1169 us, the MLA gather 175 -> 170
+// us, the stress gather 41.6 -> 40.8 us, the SWA gather unchanged (22.5 us).
+#ifndef GTKV_FAN_TABLE
+#define GTKV_FAN_TABLE 1  // 0: gathers without a plan keep the vector kernel
+#endif
+#ifndef GTKV_FAN_TABLE_GROUP
+#define GTKV_FAN_TABLE_GROUP 1  // table entries per block in table order
+#endif
 // Bytes the load barrier expects beyond what the loads deliver: 0, except in
 // the test build that checks the bounded wait (its loads never "land").
 #ifndef GTKV_FAN_TEST_EXTRA_TX
@@ -304,6 +316,7 @@ __global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const
 #endif
 
 static_assert(GTKV_FAN_GROUP >= 1 && GTKV_FAN_GROUP <= 32, "one warp per block");
+static_assert(GTKV_FAN_TABLE_GROUP >= 1 && GTKV_FAN_TABLE_GROUP <= 32, "one warp per block");
 constexpr uint32_t kFanSpinLimit = 1u << 24;  // barrier polls before a load is given up on (~1 s)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -353,17 +366,19 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
   check_gather_meta(p, n_seqs, max_pages, seq_start, seq_len, cu, out_rows, tid,
                     static_cast<int64_t>(gridDim.x) * 32);
   const int64_t n_entries = static_cast<int64_t>(n_seqs) * max_pages;
-  const int32_t flags = __ldg(plan + 3);
-  if (__ldg(plan + 1) != n_seqs || __ldg(plan + 2) != max_pages || ((flags & kPlanKernelFacing) != 0) != KF) {
-    if (tid == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
-    return;
-  }
-  int64_t n_units = n_entries;
+  int64_t n_units = n_entries;  // table order, unless a page-major plan is given
   const int32_t* order = nullptr;
-  if (flags & kPlanPageMajor) {
-    const int64_t np = __ldg(plan);
-    n_units = np < 0 ? 0 : (np > n_entries ? n_entries : np);
-    order = plan + kPlanHeaderWords + p.num_pages + 1;
+  if (plan != nullptr) {
+    const int32_t flags = __ldg(plan + 3);
+    if (__ldg(plan + 1) != n_seqs || __ldg(plan + 2) != max_pages || ((flags & kPlanKernelFacing) != 0) != KF) {
+      if (tid == 0) atomicOr(p.err, KV_DEV_ERR_TABLE);
+      return;
+    }
+    if (flags & kPlanPageMajor) {
+      const int64_t np = __ldg(plan);
+      n_units = np < 0 ? 0 : (np > n_entries ? n_entries : np);
+      order = plan + kPlanHeaderWords + p.num_pages + 1;
+    }
   }
   const int64_t vpr = p.vpr;
   const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * p.ps;
@@ -489,12 +504,14 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
   const bool latent = p.kv_rows == 1;
   const int64_t page_layer_bytes = static_cast<int64_t>(p.kv_rows) * p.ps * p.vpr * 16;
   const int64_t n_table = static_cast<int64_t>(n_seqs) * max_pages;
-  if (GTKV_GATHER_FANOUT && plan != nullptr && page_layer_bytes <= GTKV_FAN_MAX_BYTES && n_table >= p.num_pages) {
+  const bool fan_planned = plan != nullptr && n_table >= p.num_pages;
+  const bool fan_table = plan == nullptr && GTKV_FAN_TABLE;
+  if (GTKV_GATHER_FANOUT && page_layer_bytes <= GTKV_FAN_MAX_BYTES && (fan_planned || fan_table)) {
     using FanKernel = decltype(&k_gather_fan<true, false>);
     const FanKernel fans[2][2] = {{k_gather_fan<true, false>, k_gather_fan<true, true>},
                                   {k_gather_fan<false, false>, k_gather_fan<false, true>}};
     const FanKernel fan = fans[latent][kernel_facing];
-    constexpr int group = GTKV_FAN_GROUP;
+    const int group = plan != nullptr ? GTKV_FAN_GROUP : GTKV_FAN_TABLE_GROUP;
     // page buffers per block: as many as GTKV_FAN_MAX_BYTES holds, at most one per position
     int64_t nbuf = GTKV_FAN_MAX_BYTES / page_layer_bytes;
     if (nbuf > group) nbuf = group;

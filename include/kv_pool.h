@@ -84,9 +84,9 @@ enum {
                               pair skipped);
                               kernel-facing gather / plan: an entry was not a multiple of 2L
                               (its tokens skipped) */
-#define KV_DEV_ERR_TIMEOUT 16 /* planned gather: a page load into shared memory did not complete
-                                 within its bounded wait (~1 s); that block's remaining rows
-                                 are left untouched. Not expected on a healthy GPU. */
+#define KV_DEV_ERR_TIMEOUT 16 /* gather: a page load into shared memory did not complete within
+                                 its bounded wait (~1 s); that block's remaining rows are left
+                                 untouched. Not expected on a healthy GPU. */
 
 typedef struct kv_pool kv_pool_t; /* opaque, host-side, owned by the library */
 
@@ -267,7 +267,11 @@ int kv_store_all_layers_slots(const kv_pool_t* pool, const int64_t* slots_dev, i
  * len_s > max_pages * ps, cu_out[s] < 0, cu_out[s+1] < cu_out[s] or a span
  * shorter than its token count, or when cu_out[n_seqs] > out_rows (rows past
  * out_rows are not written); KV_DEV_ERR_ROW when a page is >= num_pages (that
- * token is skipped). Every access stays in bounds whatever the metadata. */
+ * token is skipped). Every access stays in bounds whatever the metadata.
+ * Where one page's rows of a layer (ps * 2R bytes, ps * R for MLA) fit in
+ * 72 KiB, each table entry's rows are staged in shared memory by bulk copy and
+ * bulk-copied out, with a bounded wait for the load (KV_DEV_ERR_TIMEOUT);
+ * otherwise warps copy them through registers. The output is the same. */
 int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_table_dev, int32_t n_seqs,
                     int32_t max_pages, const int32_t* seq_start_dev, const int32_t* seq_len_dev,
                     const int64_t* cu_out_dev, void* out_k_dev, void* out_v_dev, int64_t out_rows,

@@ -1,6 +1,6 @@
-"""The bounded wait of the fan-out planned gather, made to run out on purpose.
+"""The bounded wait of the fan-out gather, made to run out on purpose.
 
-The fan-out form of kv_gather_layer_planned stages each page in shared memory
+The fan-out form of kv_gather_layer_planned and kv_gather_layer stages pages in shared memory
 with bulk copies whose completion it counts on an mbarrier, polling at most a
 fixed number of times (about a second). A build with
 GTKV_FAN_TEST_EXTRA_TX=16 makes that barrier expect 16 bytes more than the
@@ -73,6 +73,12 @@ def test_fan_gather_wait_runs_out_cleanly(variant):
         assert err.value == gt.KV_DEV_ERR_TIMEOUT
         assert bool((out_k == 0x5A).all()) and bool((out_v == 0x5A).all())  # no block wrote a row
         assert waited < 60
+        # the gather without a plan (table order, one entry per block) takes the same wait
+        _ok(L.kv_gather_layer(pool, 0, p(bt), 2, 2, None, p(ln), p(cu), p(out_k), p(out_v), 4 * ps, stream))
+        torch.cuda.synchronize()
+        _ok(L.kv_pool_last_error(pool, stream, ctypes.byref(err)))
+        assert err.value == gt.KV_DEV_ERR_TIMEOUT
+        assert bool((out_k == 0x5A).all()) and bool((out_v == 0x5A).all())
         # the context is still usable: a translate on the same pool and stream
         slots = torch.tensor([9, 17, -1], dtype=torch.int64, device="cuda")
         ids = torch.empty(3, dtype=torch.int32, device="cuda")
