@@ -96,6 +96,7 @@ int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, k
   if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return KV_ERR_CUDA;
+  if (gtkv::prepare_gather() != cudaSuccess) return KV_ERR_CUDA;
   if (raw_dev != nullptr) {
     // a borrowed buffer must be device (or managed) memory of this device:
     // anything else would only show up later, as a fault in a kernel

@@ -494,6 +494,22 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
 
 }  // namespace
 
+// The fan-out kernels take up to GTKV_FAN_MAX_BYTES of dynamic shared memory,
+// more than the 48 KiB a launch gets by default; the limit is a property of
+// the function on the current device, raised here once per pool (from
+// kv_pool_create, outside any stream capture) so that no launch has to.
+cudaError_t prepare_gather() {
+  const void* fans[] = {reinterpret_cast<const void*>(k_gather_fan<true, false>),
+                        reinterpret_cast<const void*>(k_gather_fan<true, true>),
+                        reinterpret_cast<const void*>(k_gather_fan<false, false>),
+                        reinterpret_cast<const void*>(k_gather_fan<false, true>)};
+  for (const void* f : fans) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, GTKV_FAN_MAX_BYTES);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
                           const int32_t* seq_start, const int32_t* seq_len, const int64_t* cu, void* out_k,
                           void* out_v, int64_t out_rows, const int32_t* plan, bool kernel_facing, int sm_count,
@@ -516,11 +532,7 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
     int64_t nbuf = GTKV_FAN_MAX_BYTES / page_layer_bytes;
     if (nbuf > group) nbuf = group;
     if (nbuf < 1) nbuf = 1;
-    const int smem = static_cast<int>(nbuf * page_layer_bytes);
-    if (smem > 48 * 1024) {
-      const cudaError_t e = cudaFuncSetAttribute(fan, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-    }
+    const int smem = static_cast<int>(nbuf * page_layer_bytes);  // <= GTKV_FAN_MAX_BYTES: see prepare_gather
     int64_t blocks = (n_table + group - 1) / group;
     const int64_t seq_blocks = (static_cast<int64_t>(n_seqs) + 31) / 32;  // the metadata checks
     if (blocks < seq_blocks) blocks = seq_blocks;

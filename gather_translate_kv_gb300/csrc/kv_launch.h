@@ -13,6 +13,8 @@ cudaError_t launch_store(const DevPool& p, int32_t layer0, int32_t n_layers, con
 cudaError_t launch_store_slots(const DevPool& p, int32_t layer0, int32_t n_layers, const int64_t* slots, int64_t n,
                                const int32_t* v2p, int64_t v2p_len, const void* k, const void* v, int sm_count,
                                cudaStream_t s);
+// Per-device set-up of the gather kernels (their shared-memory limit); called by kv_pool_create.
+cudaError_t prepare_gather();
 cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, int32_t n_seqs, int32_t max_pages,
                           const int32_t* seq_start, const int32_t* seq_len, const int64_t* cu, void* out_k,
                           void* out_v, int64_t out_rows, const int32_t* plan, bool kernel_facing, int sm_count,

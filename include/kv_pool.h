@@ -151,7 +151,10 @@ int kv_pool_required_bytes(const kv_pool_desc* desc, int64_t* total_bytes, int64
  *    bytes always suffices.
  * Additionally requires R % 16 == 0 and anchor_bytes % 16 == 0
  * (KV_ERR_ALIGN): every kernel moves rows as 16-byte vectors.
- * Also allocates the pool's device error word (8 bytes). Launches no kernel.
+ * Also allocates the pool's device error word (8 bytes) and raises the
+ * gather kernels' shared-memory limit on the current device (a property of
+ * the functions, set here so that no later call has to; create pools outside
+ * stream capture). Launches no kernel.
  * On success *out receives the handle; on failure *out is set to NULL and
  * nothing stays allocated. */
 int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, kv_pool_t** out);

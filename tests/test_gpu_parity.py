@@ -379,7 +379,9 @@ def test_gather_tombstoned_table_entry_reads_sink():
 
 def test_calls_capture_in_a_cuda_graph():
     """translate -> store -> gather, and plan -> planned gather, captured once,
-    replayed on new inputs."""
+    replayed on new inputs. The pages hold 64 KiB of K and V per layer and the
+    table has more entries than the pool has pages, so both gathers run their
+    fan-out form (bulk copies through 64 KiB of shared memory) inside the graph."""
     shape = synth.SHAPES[2].scaled(24)
     pp = PoolPair(shape)
     o, R, ps, P = pp.o, pp.R, shape.page_size, shape.num_pages
@@ -389,8 +391,9 @@ def test_calls_capture_in_a_cuda_graph():
     ids_d = torch.zeros(n, dtype=torch.int32, device="cuda")
     k_d = torch.zeros((n, R), dtype=torch.uint8, device="cuda")
     v_d = torch.zeros_like(k_d)
-    bt = np.stack([1 + np.arange(8) + 8 * s for s in range(2)]).astype(np.int32)
-    g = synth.GatherBatch(bt, np.zeros(2, np.int32), np.full(2, 8 * ps, np.int32))
+    bt = np.stack([1 + np.arange(8) + 2 * s for s in range(4)]).astype(np.int32)  # 14 pages, 32 entries: page-major
+    assert bt.size >= P and 2 * ps * R == 65536
+    g = synth.GatherBatch(bt, np.zeros(4, np.int32), np.full(4, 8 * ps, np.int32))
     bt_d, ln_d, cu_d = to_dev(bt), to_dev(g.seq_len), to_dev(g.cu)
     ok_d = torch.zeros((g.total, R), dtype=torch.uint8, device="cuda")
     ov_d = torch.zeros_like(ok_d)
