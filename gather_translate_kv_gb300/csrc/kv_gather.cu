@@ -21,9 +21,9 @@
 //
 // Where one page's rows of a layer fit in 72 KiB of shared memory, gathers take
 // the fan-out form instead (k_gather_fan, below): a block stages each page it
-// needs once in shared memory and bulk-copies it to its readers -- with a plan
-// (over tables of at least num_pages entries) all readers of a page in its
-// positions, without one a single table entry.
+// needs once in shared memory and bulk-copies it to its readers -- with a
+// page-major plan over a table of at least num_pages entries, the readers of
+// a page among its two plan positions; otherwise a single table entry.
 #include "kv_launch.h"
 #include "kv_plan.cuh"
 
@@ -282,32 +282,27 @@ __global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const
 // pages keeps up to `nbuf` page loads in flight (one buffer and one mbarrier
 // each), issued in the order the pages are written.
 //
-// Measured on the decode gather (256 x 4096 tokens over tables that name every
-// page ~16 times): 742 -> 708 us against the vector kernel's page-major walk;
-// 2 positions per block is as fast as 3 or 4 there and the best on the MLA
-// gather (142 -> 131 us). Where pages are read once a block of two entries
-// ends with the later of two loads, which cost the SWA gather 5 %; so the
-// launcher takes this form only for tables with at least as many entries as
-// the pool has pages, where the page-major walk is the one that pays.
+// Positions per block, measured: on the decode gather (256 x 4096 tokens over
+// tables that name every page ~16 times) 2 positions per block take the
+// page-major walk from 742 to 708 us against the vector kernel (3 or 4: the
+// same; 1: 757 us, every reader reloading its page) and the MLA gather from 142
+// to 131 us. Where pages are read about once, a block of two entries ends with
+// the later of two loads (the SWA gather +5 %), and one entry per block is as
+// fast as the vector kernel or faster (stress gather 42.1 -> 41.0 us). So a
+// block takes 2 positions when the table has at least as many entries as the
+// pool has pages (its entries then name pages several times over), else 1;
+// gathers without a plan take 1 table entry per block (decode tables 1241 ->
+// 1169 us, MLA 175 -> 170 us, stress 41.6 -> 40.8 us, SWA unchanged). Pages
+// whose rows of a layer exceed GTKV_FAN_MAX_BYTES keep the vector kernel.
 
 #ifndef GTKV_GATHER_FANOUT
-#define GTKV_GATHER_FANOUT 1  // 0: planned gathers always take the vector kernel
+#define GTKV_GATHER_FANOUT 1  // 0: every gather takes the vector kernel
 #endif
 #ifndef GTKV_FAN_GROUP
-#define GTKV_FAN_GROUP 2  // plan positions per block (1..32)
+#define GTKV_FAN_GROUP 2  // plan positions per block for tables of >= num_pages entries (1..32)
 #endif
 #ifndef GTKV_FAN_MAX_BYTES
 #define GTKV_FAN_MAX_BYTES 73728  // shared memory per block for page buffers (a 64-row 1152-byte latent page)
-#endif
-// Gathers without a plan take the same kernel in table order, one entry per
-// block (a block of one entry waits for one load only): on the decode tables,
-// whose pages are named ~16 times, 1241 -> 1169 us, the MLA gather 175 -> 170
-// us, the stress gather 41.6 -> 40.8 us, the SWA gather unchanged (22.5 us).
-#ifndef GTKV_FAN_TABLE
-#define GTKV_FAN_TABLE 1  // 0: gathers without a plan keep the vector kernel
-#endif
-#ifndef GTKV_FAN_TABLE_GROUP
-#define GTKV_FAN_TABLE_GROUP 1  // table entries per block in table order
 #endif
 // Bytes the load barrier expects beyond what the loads deliver: 0, except in
 // the test build that checks the bounded wait (its loads never "land").
@@ -316,7 +311,6 @@ __global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const
 #endif
 
 static_assert(GTKV_FAN_GROUP >= 1 && GTKV_FAN_GROUP <= 32, "one warp per block");
-static_assert(GTKV_FAN_TABLE_GROUP >= 1 && GTKV_FAN_TABLE_GROUP <= 32, "one warp per block");
 constexpr uint32_t kFanSpinLimit = 1u << 24;  // barrier polls before a load is given up on (~1 s)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -520,14 +514,12 @@ cudaError_t launch_gather(const DevPool& p, int32_t layer, const int32_t* bt, in
   const bool latent = p.kv_rows == 1;
   const int64_t page_layer_bytes = static_cast<int64_t>(p.kv_rows) * p.ps * p.vpr * 16;
   const int64_t n_table = static_cast<int64_t>(n_seqs) * max_pages;
-  const bool fan_planned = plan != nullptr && n_table >= p.num_pages;
-  const bool fan_table = plan == nullptr && GTKV_FAN_TABLE;
-  if (GTKV_GATHER_FANOUT && page_layer_bytes <= GTKV_FAN_MAX_BYTES && (fan_planned || fan_table)) {
+  if (GTKV_GATHER_FANOUT && page_layer_bytes <= GTKV_FAN_MAX_BYTES) {
     using FanKernel = decltype(&k_gather_fan<true, false>);
     const FanKernel fans[2][2] = {{k_gather_fan<true, false>, k_gather_fan<true, true>},
                                   {k_gather_fan<false, false>, k_gather_fan<false, true>}};
     const FanKernel fan = fans[latent][kernel_facing];
-    const int group = plan != nullptr ? GTKV_FAN_GROUP : GTKV_FAN_TABLE_GROUP;
+    const int group = plan != nullptr && n_table >= p.num_pages ? GTKV_FAN_GROUP : 1;
     // page buffers per block: as many as GTKV_FAN_MAX_BYTES holds, at most one per position
     int64_t nbuf = GTKV_FAN_MAX_BYTES / page_layer_bytes;
     if (nbuf > group) nbuf = group;

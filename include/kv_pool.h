@@ -314,12 +314,13 @@ int kv_gather_layer(const kv_pool_t* pool, int32_t layer, const int32_t* block_t
  *   the output is identical. A plan built for another table shape, or from
  *   a kernel-facing table, sets KV_DEV_ERR_TABLE and writes nothing; plan
  *   entries are bounds-checked one by one, so a stale or foreign plan never
- *   reads outside its buffer. Two kernels implement it, with the same
- *   output: when n_seqs * max_pages >= num_pages and one page's rows of a
- *   layer (ps * 2R bytes, ps * R for MLA) fit in 72 KiB, blocks of two plan
- *   positions stage each page once in shared memory and bulk-copy it to its
- *   readers (its waits for those loads are bounded: KV_DEV_ERR_TIMEOUT);
- *   otherwise warps copy the rows through registers. */
+ *   reads outside its buffer. Where one page's rows of a layer (ps * 2R
+ *   bytes, ps * R for MLA) fit in 72 KiB, blocks of one warp stage each page
+ *   once in shared memory and bulk-copy it to their readers (bounded waits
+ *   for those loads: KV_DEV_ERR_TIMEOUT), two plan positions per block when
+ *   n_seqs * max_pages >= num_pages (pages are then named several times
+ *   over), one otherwise; larger pages are copied through registers by
+ *   warps. The output is the same. */
 int kv_gather_plan_bytes(const kv_pool_t* pool, int32_t n_seqs, int32_t max_pages, int64_t* plan_bytes);
 int kv_gather_plan(const kv_pool_t* pool, const int32_t* block_table_dev, int32_t n_seqs, int32_t max_pages,
                    const int32_t* seq_start_dev, const int32_t* seq_len_dev, void* plan_dev, int64_t plan_bytes,

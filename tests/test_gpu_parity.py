@@ -840,13 +840,13 @@ def test_planned_gather_matches_oracle(shape, anchor, latent):
                                                  (MLA_SHAPES[0][0], 0, True)],
                          ids=["R2048-ps16", "odd-rows", "R64-ps256", "mla-r1152"])
 def test_planned_gather_both_forms(shape, anchor, latent):
-    """kv_gather_layer_planned has two kernels with one output: blocks that
-    stage each page in shared memory and bulk-copy it to its readers (tables
-    of at least num_pages entries, when one page's rows of a layer fit in
-    72 KiB) and warps that copy through registers (smaller tables). The same
-    pool read through a table on each side of that rule, with shared pages,
-    tombstoned entries, windows starting mid-page and gaps between the
-    output spans, must equal the oracle's gather, in both table forms."""
+    """kv_gather_layer_planned stages pages in shared memory and bulk-copies
+    them to their readers (pages of at most 72 KiB per layer, as here), with
+    two plan positions per block for tables of at least num_pages entries and
+    one below that. The same pool read through a table on each side of that
+    rule, with shared pages, tombstoned entries, windows starting mid-page and
+    gaps between the output spans, must equal the oracle's gather, in both
+    table forms, and so must the gather without a plan."""
     rng = np.random.default_rng(700 + shape.row_bytes)
     pp = PoolPair(shape, anchor, latent=latent)
     o, R, L, ps, P = pp.o, pp.R, shape.layer_num, shape.page_size, shape.num_pages
@@ -879,8 +879,18 @@ def test_planned_gather_both_forms(shape, anchor, latent):
                 fn = gt.kv_gather_layer_planned_kf if form == "kernel-facing" else gt.kv_gather_layer_planned
                 fn(pp.pool, layer, plan, to_dev(table), to_dev(ln), to_dev(cu), dk, dv, to_dev(st))
                 assert pp.last_error() == 0
-                what = f"{'fan-out' if fan else 'vector'} planned gather, {form} table, layer {layer}"
+                what = f"planned gather ({2 if fan else 1} positions per block), {form} table, layer {layer}"
                 assert_bytes_equal(dk.cpu().numpy(), ok, what + " K", R)
                 if not latent:
                     assert_bytes_equal(dv.cpu().numpy(), ov, what + " V", R)
+                dk.fill_(0x11)
+                if not latent:
+                    dv.fill_(0x22)
+                fn = gt.kv_gather_layer_kf if form == "kernel-facing" else gt.kv_gather_layer
+                fn(pp.pool, layer, to_dev(table), to_dev(ln), to_dev(cu), dk, dv, to_dev(st))
+                assert pp.last_error() == 0
+                assert_bytes_equal(dk.cpu().numpy(), ok, f"gather without a plan, {form} table, layer {layer} K", R)
+                if not latent:
+                    assert_bytes_equal(dv.cpu().numpy(), ov, f"gather without a plan, {form} table, layer {layer} V",
+                                       R)
     pp.close()
