@@ -190,7 +190,7 @@ def measured_hbm_peak():
 
 
 GATHER_SOURCES = [os.path.join(ROOT, "gather_translate_kv_gb300", "csrc", f)
-                  for f in ("kv_gather.cu", "kv_common.cuh", "kv_plan.cuh")]
+                  for f in ("kv_gather.cu", "kv_common.cuh", "kv_plan.cuh", "kv_bulk.cuh")]
 TRAFFIC_PROFILE = "gather_planned_decode_small_dram.txt"
 
 

@@ -24,6 +24,7 @@
 // needs once in shared memory and bulk-copies it to its readers -- with a
 // page-major plan over a table of at least num_pages entries, the readers of
 // a page among its two plan positions; otherwise a single table entry.
+#include "kv_bulk.cuh"
 #include "kv_launch.h"
 #include "kv_plan.cuh"
 
@@ -304,46 +305,7 @@ __global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const
 #ifndef GTKV_FAN_MAX_BYTES
 #define GTKV_FAN_MAX_BYTES 73728  // shared memory per block for page buffers (a 64-row 1152-byte latent page)
 #endif
-// Bytes the load barrier expects beyond what the loads deliver: 0, except in
-// the test build that checks the bounded wait (its loads never "land").
-#ifndef GTKV_FAN_TEST_EXTRA_TX
-#define GTKV_FAN_TEST_EXTRA_TX 0
-#endif
-
 static_assert(GTKV_FAN_GROUP >= 1 && GTKV_FAN_GROUP <= 32, "one warp per block");
-constexpr uint32_t kFanSpinLimit = 1u << 24;  // barrier polls before a load is given up on (~1 s)
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Polls the barrier's phase `parity` at most kFanSpinLimit times.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kFanSpinLimit; ++i)
-    if (mbar_test(bar, parity)) return true;
-  return false;
-}
-__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
-                                          uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-          "r"(smem_u32(sdst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes, uint64_t pol) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
-               "r"(smem_u32(ssrc)), "r"(bytes), "l"(pol)
-               : "memory");
-}
 
 template <bool HAS_V, bool KF>
 __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, const int32_t* __restrict__ bt,
@@ -429,17 +391,12 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
   }
   if (ng > 0) {
     const int64_t buf_vecs = p.kv_rows * p.ps * vpr;
-    if (lane < nbuf) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + lane)) : "memory");
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    if (lane < nbuf) mbar_init(bars + lane);
     __syncwarp();
     auto issue = [&](int b) {  // by the lane that leads the group
       const uint32_t bytes = static_cast<uint32_t>((g_hi - g_lo) * vpr * 16);
       uint4* sb = sbuf + b * buf_vecs;
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bars + b)),
-                   "r"((HAS_V ? 2 * bytes : bytes) + GTKV_FAN_TEST_EXTRA_TX)
-                   : "memory");
+      mbar_expect(bars + b, HAS_V ? 2 * bytes : bytes);
       const uint4* src = p.base + (g_pg * p.stride + koff + g_lo) * vpr;
       bulk_load(sb + g_lo * vpr, src, bytes, bars + b, pol.keep);
       if (HAS_V) bulk_load(sb + (p.ps + g_lo) * vpr, src + p.ps * vpr, bytes, bars + b, pol.keep);
@@ -452,7 +409,7 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
         // bounded wait, then leave
         if (lane == 0) atomicOr(p.err, KV_DEV_ERR_TIMEOUT);
         for (int q = g; q < ng && q < g + nbuf; ++q) mbar_wait_bounded(bars + q % nbuf, (q / nbuf) & 1);
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        bulk_wait_all();
         return;
       }
       if (my_g == g) {
@@ -460,10 +417,10 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
         const uint4* sb = sbuf + b * buf_vecs;
         bulk_store(out_k + mine.row * vpr, sb + off * vpr, run, pol.first);
         if (HAS_V) bulk_store(out_v + mine.row * vpr, sb + (p.ps + off) * vpr, run, pol.first);
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        bulk_commit();
       }
       if (g + nbuf < ng) {  // group g + nbuf reuses buffer b: group g's stores must have read it
-        if (my_g == g) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        if (my_g == g) bulk_wait_read();
         __syncwarp();
         if (lead_g == g + nbuf) issue(b);
       }
@@ -483,7 +440,7 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
         st16<GTKV_GATHER_ST>(out_v + row * vpr + v, ld16<GTKV_GATHER_LD>(srck + p.ps * vpr + col, pol), pol);
     }
   }
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // shared memory must outlive the stores' reads
+  bulk_wait_read();  // shared memory must outlive the stores' reads
 }
 
 }  // namespace

@@ -84,9 +84,9 @@ enum {
                               pair skipped);
                               kernel-facing gather / plan: an entry was not a multiple of 2L
                               (its tokens skipped) */
-#define KV_DEV_ERR_TIMEOUT 16 /* gather: a page load into shared memory did not complete within
-                                 its bounded wait (~1 s); that block's remaining rows are left
-                                 untouched. Not expected on a healthy GPU. */
+#define KV_DEV_ERR_TIMEOUT 16 /* gather / move: a load into shared memory did not complete
+                                 within its bounded wait (~1 s); that block's remaining rows
+                                 are left untouched. Not expected on a healthy GPU. */
 
 typedef struct kv_pool kv_pool_t; /* opaque, host-side, owned by the library */
 
@@ -369,7 +369,9 @@ int kv_gather_plan_noalloc(const kv_pool_t* pool, const int32_t* block_table_dev
  * distinct; otherwise the result is unspecified (still in bounds).
  * Device errors: an id outside [0, n_rows) sets KV_DEV_ERR_ROW and an id
  * whose offset id % (ps*2L) is >= ps sets KV_DEV_ERR_FORM; that pair is
- * skipped. */
+ * skipped. Pairs of at most 36 KiB (2L rows of R bytes, R >= 128) are copied
+ * through shared memory by bulk copies, with a bounded wait for the loads
+ * (KV_DEV_ERR_TIMEOUT); others row by row through registers. */
 int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* dst_ids_dev, int64_t n,
             kv_stream_t stream);
 
