@@ -268,7 +268,7 @@ __global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const
   }
 }
 
-// ---- fan-out form of the planned gather ----------------------------------
+// ---- fan-out form of the gather -------------------------------------------
 //
 // With a page-major plan the readers of a page are consecutive plan
 // positions. A block of one warp takes `group` consecutive positions (whole

@@ -837,21 +837,27 @@ def test_planned_gather_matches_oracle(shape, anchor, latent):
 
 @pytest.mark.parametrize("shape,anchor,latent", [(synth.SHAPES[2].scaled(40), 0, False), (SHAPES[5][0], 16, False),
                                                  (synth.SHAPES[5].scaled(20), 0, False),
-                                                 (MLA_SHAPES[0][0], 0, True)],
-                         ids=["R2048-ps16", "odd-rows", "R64-ps256", "mla-r1152"])
+                                                 (MLA_SHAPES[0][0], 0, True),
+                                                 (S(0, "mla-r1152-ps128", 3, 1, 576, 2, 128, 12), 0, True),
+                                                 (S(0, "mla-r512-ps256", 2, 1, 256, 2, 256, 10), 16, True),
+                                                 (S(0, "r2048-ps64", 2, 8, 128, 2, 64, 12), 0, False)],
+                         ids=["R2048-ps16", "odd-rows", "R64-ps256", "mla-r1152", "mla-r1152-ps128-vector",
+                              "mla-r512-ps256-vector", "R2048-ps64-vector"])
 def test_planned_gather_both_forms(shape, anchor, latent):
-    """kv_gather_layer_planned stages pages in shared memory and bulk-copies
-    them to their readers (pages of at most 72 KiB per layer, as here), with
-    two plan positions per block for tables of at least num_pages entries and
-    one below that. The same pool read through a table on each side of that
-    rule, with shared pages, tombstoned entries, windows starting mid-page and
-    gaps between the output spans, must equal the oracle's gather, in both
-    table forms, and so must the gather without a plan."""
+    """Where a page holds at most 72 KiB per layer (the first four shapes)
+    the gathers stage pages in shared memory and bulk-copy them to their
+    readers, with two plan positions per block for tables of at least
+    num_pages entries and one below that; larger pages (the last three,
+    including the 1152-byte latent rows' own vector rounds) are copied by warps
+    through registers. The same pool read through a table on each side of the
+    table-size rule, with shared pages, tombstoned entries, windows starting
+    mid-page and gaps between the output spans, must equal the oracle's
+    gather, in both table forms, planned and not."""
     rng = np.random.default_rng(700 + shape.row_bytes)
     pp = PoolPair(shape, anchor, latent=latent)
     o, R, L, ps, P = pp.o, pp.R, shape.layer_num, shape.page_size, shape.num_pages
     B = pp.pool.info["blocks_per_page"]
-    assert (2 - latent) * ps * R <= 73728
+    staged = (2 - latent) * ps * R <= 73728
     maxp = min(P - 1, 6)
     for S_ in (-(-P // maxp) + 3, max(1, (P - 1) // maxp)):  # n_seqs * max_pages >= P, then < P
         fan = S_ * maxp >= P
@@ -879,7 +885,8 @@ def test_planned_gather_both_forms(shape, anchor, latent):
                 fn = gt.kv_gather_layer_planned_kf if form == "kernel-facing" else gt.kv_gather_layer_planned
                 fn(pp.pool, layer, plan, to_dev(table), to_dev(ln), to_dev(cu), dk, dv, to_dev(st))
                 assert pp.last_error() == 0
-                what = f"planned gather ({2 if fan else 1} positions per block), {form} table, layer {layer}"
+                what = (f"planned gather ({2 if fan else 1} positions per block), " if staged else
+                        "planned gather (vector kernel), ") + f"{form} table, layer {layer}"
                 assert_bytes_equal(dk.cpu().numpy(), ok, what + " K", R)
                 if not latent:
                     assert_bytes_equal(dv.cpu().numpy(), ov, what + " V", R)
