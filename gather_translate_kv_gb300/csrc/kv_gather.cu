@@ -305,6 +305,14 @@ __global__ void GTKV_GATHER_BOUNDS k_gather_runs(DevPool p, int32_t layer, const
 #ifndef GTKV_FAN_MAX_BYTES
 #define GTKV_FAN_MAX_BYTES 73728  // shared memory per block for page buffers (a 64-row 1152-byte latent page)
 #endif
+// L2 eviction priority of the page loads (pages have other readers in
+// nearby blocks) and of the output stores (never read back by the gather).
+#ifndef GTKV_FAN_LD_PRIO
+#define GTKV_FAN_LD_PRIO "evict_last"
+#endif
+#ifndef GTKV_FAN_ST_PRIO
+#define GTKV_FAN_ST_PRIO "evict_first"
+#endif
 static_assert(GTKV_FAN_GROUP >= 1 && GTKV_FAN_GROUP <= 32, "one warp per block");
 
 template <bool HAS_V, bool KF>
@@ -339,6 +347,9 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
   const int64_t vpr = p.vpr;
   const int64_t koff = static_cast<int64_t>(layer) * p.kv_rows * p.ps;
   const L2Policy pol = make_l2_policy();
+  uint64_t ld_pol, st_pol;
+  asm("createpolicy.fractional.L2::" GTKV_FAN_LD_PRIO ".b64 %0, 1.0;" : "=l"(ld_pol));
+  asm("createpolicy.fractional.L2::" GTKV_FAN_ST_PRIO ".b64 %0, 1.0;" : "=l"(st_pol));
 
   // lane j < group: plan position blockIdx.x * group + j, a whole table entry
   Run mine{0, 0, 0, 0};
@@ -398,8 +409,8 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
       uint4* sb = sbuf + b * buf_vecs;
       mbar_expect(bars + b, HAS_V ? 2 * bytes : bytes);
       const uint4* src = p.base + (g_pg * p.stride + koff + g_lo) * vpr;
-      bulk_load(sb + g_lo * vpr, src, bytes, bars + b, pol.keep);
-      if (HAS_V) bulk_load(sb + (p.ps + g_lo) * vpr, src + p.ps * vpr, bytes, bars + b, pol.keep);
+      bulk_load(sb + g_lo * vpr, src, bytes, bars + b, ld_pol);
+      if (HAS_V) bulk_load(sb + (p.ps + g_lo) * vpr, src + p.ps * vpr, bytes, bars + b, ld_pol);
     };
     if (lead_g >= 0 && lead_g < nbuf) issue(lead_g);
     for (int g = 0; g < ng; ++g) {
@@ -415,8 +426,8 @@ __global__ void __launch_bounds__(32) k_gather_fan(DevPool p, int32_t layer, con
       if (my_g == g) {
         const uint32_t run = static_cast<uint32_t>(nrows * vpr * 16);
         const uint4* sb = sbuf + b * buf_vecs;
-        bulk_store(out_k + mine.row * vpr, sb + off * vpr, run, pol.first);
-        if (HAS_V) bulk_store(out_v + mine.row * vpr, sb + (p.ps + off) * vpr, run, pol.first);
+        bulk_store(out_k + mine.row * vpr, sb + off * vpr, run, st_pol);
+        if (HAS_V) bulk_store(out_v + mine.row * vpr, sb + (p.ps + off) * vpr, run, st_pol);
         bulk_commit();
       }
       if (g + nbuf < ng) {  // group g + nbuf reuses buffer b: group g's stores must have read it
