@@ -42,6 +42,14 @@ int enter(const kv_pool_t* pool) {
 
 int launched(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
 
+// A runtime call of pool set-up failed: take its error out of the runtime's
+// last-error slot (it would otherwise surface as the status of the next
+// launch, through cudaGetLastError) and report KV_ERR_CUDA.
+int failed_call() {
+  cudaGetLastError();
+  return KV_ERR_CUDA;
+}
+
 // The pool's device words: [0] the error word the kernels OR bits into,
 // [1] where kv_pool_last_error parks the value it took.
 constexpr size_t kErrWords = 2;
@@ -93,10 +101,10 @@ int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, k
   }
 
   int dev = -1, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) return failed_call();
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-    return KV_ERR_CUDA;
-  if (gtkv::prepare_gather() != cudaSuccess) return KV_ERR_CUDA;
+    return failed_call();
+  if (gtkv::prepare_gather() != cudaSuccess) return failed_call();
   if (raw_dev != nullptr) {
     // a borrowed buffer must be device (or managed) memory of this device:
     // anything else would only show up later, as a fault in a kernel
@@ -122,7 +130,7 @@ int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, k
     void* mem = nullptr;
     if (cudaMalloc(&mem, static_cast<size_t>(lay.alloc_bytes)) != cudaSuccess) {
       delete p;
-      return KV_ERR_CUDA;
+      return failed_call();
     }
     p->raw = static_cast<uint8_t*>(mem);
     p->raw_bytes = lay.alloc_bytes;
@@ -138,7 +146,7 @@ int kv_pool_create(const kv_pool_desc* desc, void* raw_dev, int64_t raw_bytes, k
     if (err) cudaFree(err);
     if (p->owns_raw) cudaFree(p->raw);
     delete p;
-    return KV_ERR_CUDA;
+    return failed_call();
   }
   p->d_err = static_cast<int32_t*>(err);
 

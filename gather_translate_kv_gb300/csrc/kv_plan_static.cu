@@ -152,7 +152,10 @@ extern "C" int kv_gather_plan_noalloc(const kv_pool_t* pool, const int32_t* bloc
       (reinterpret_cast<uintptr_t>(block_table_dev) & 3u) || (reinterpret_cast<uintptr_t>(seq_start_dev) & 3u))
     return KV_ERR_ALIGN;
   int32_t* counts = nullptr;
-  if (counts_on(device, &counts) != cudaSuccess) return KV_ERR_CUDA;
+  if (counts_on(device, &counts) != cudaSuccess) {
+    cudaGetLastError();  // a failed look-up must not surface as the status of a later launch
+    return KV_ERR_CUDA;
+  }
 
   nvtxRangePushA("kv_gather_plan_noalloc");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -741,6 +741,23 @@ def test_mla_path_matches_oracle(shape, anchor):
     pp.close()
 
 
+def test_failed_create_leaves_no_pending_error():
+    """A pool the device cannot hold (2 TB of 64 KiB rows): kv_pool_create
+    returns KV_ERR_CUDA, allocates nothing, and the failed allocation does not
+    surface as the status of the next launch on another pool."""
+    huge = gt.make_desc(1, 64, 256, 4, 16, 1 << 20)  # n_rows = 2^25 < 2^31, 64 KiB rows
+    total, _ = gt.kv_pool_required_bytes(huge)
+    assert total >= 1 << 41
+    with pytest.raises(gt.KVError) as e:
+        gt.kv_pool_create(huge)
+    assert e.value.name == "KV_ERR_CUDA"
+    pool = gt.kv_pool_create(gt.make_desc(2, 2, 8, 2, 4, 8))
+    ids = torch.empty(2, dtype=torch.int32, device="cuda")
+    gt.kv_translate(pool, torch.tensor([5, -1], dtype=torch.int64, device="cuda"), ids)
+    assert ids.cpu().tolist() == [1 * 16 + 1, 0] and gt.kv_pool_last_error(pool) == 0
+    gt.kv_pool_destroy(pool)
+
+
 def test_library_owned_buffer_round_trip():
     """kv_pool_create without a buffer: the library allocates anchor + total +
     tail pad bytes itself; a store then a gather returns the stored rows, and
