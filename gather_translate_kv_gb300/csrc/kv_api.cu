@@ -40,7 +40,14 @@ int enter(const kv_pool_t* pool) {
   return dev == pool->device ? KV_OK : KV_ERR_DEVICE;
 }
 
-int launched(cudaError_t e) { return e == cudaSuccess ? KV_OK : KV_ERR_CUDA; }
+// Status of an enqueue. A failed runtime call also leaves its error in the
+// runtime's last-error slot, where the next launch's check would find it;
+// take it out so that it is reported once, here.
+int launched(cudaError_t e) {
+  if (e == cudaSuccess) return KV_OK;
+  cudaGetLastError();
+  return KV_ERR_CUDA;
+}
 
 // A runtime call of pool set-up failed: take its error out of the runtime's
 // last-error slot (it would otherwise surface as the status of the next
