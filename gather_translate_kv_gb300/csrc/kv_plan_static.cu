@@ -174,5 +174,7 @@ extern "C" int kv_gather_plan_noalloc(const kv_pool_t* pool, const int32_t* bloc
   }
   if (e == cudaSuccess) e = cudaMemcpyAsync(plan + kPlanHeaderWords, counts, count_bytes, cudaMemcpyDeviceToDevice, s);
   nvtxRangePop();
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  if (e == cudaSuccess) return KV_OK;
+  cudaGetLastError();  // reported here, not again by a later launch
+  return KV_ERR_CUDA;
 }
