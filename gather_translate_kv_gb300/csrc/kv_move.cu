@@ -8,8 +8,8 @@
 // consecutive tasks, so the 2L rows of a pair are spread over consecutive row
 // groups. Sources and destinations are disjoint by precondition, so loads use
 // the coherent path (the pool is written by this kernel) and need no ordering.
-// Pairs of at most 36 KiB with rows of at least 128 bytes take the bulk-copy
-// form below instead (one warp per pair, through shared memory).
+// Rows of at least 128 bytes take the bulk-copy form below instead (one warp
+// per pair, or per chunk of at most 36 KiB of it, through shared memory).
 #include "kv_bulk.cuh"
 #include "kv_launch.h"
 #include "kv_tasks.cuh"
@@ -87,15 +87,19 @@ __global__ void __launch_bounds__(kBlock) k_move(DevPool p, const int32_t* __res
   }
 }
 
-// Bulk-copy form: one block of one warp per pair (grid-stride beyond the
-// grid). Lane j issues the bulk loads of rows j, j + 32, ... of token src into
-// shared memory, counted on one mbarrier, and once they have landed their bulk
-// stores to the same rows of token dst. Measured against the vector kernel
-// over 8192 random pairs on 2 GB pools (µs): rows of 128 to 2048 bytes with up
-// to 36 KiB per pair 2-10 % faster (512-byte rows x 24 row-blocks 74.7 -> 70.8,
-// the SWA move 67.7 -> 63.9); 64 to 72 KiB per pair (3 pairs in flight per SM)
-// the same or up to 12 % slower; 64-byte rows 15 % slower. So the launcher
-// takes it for rows of at least 128 bytes and pairs of at most 36 KiB.
+// Bulk-copy form: one block of one warp per pair, or per chunk of a pair's
+// row-blocks when the pair holds more than GTKV_MOVE_BULK_MAX_BYTES (grid-
+// stride beyond the grid). Lane j issues the bulk loads of rows b0 + j,
+// b0 + j + 32, ... of token src into shared memory, counted on one mbarrier,
+// and once they have landed their bulk stores to the same rows of token dst.
+// Measured against the vector kernel over 8192 random pairs on 2 GB pools
+// (us): rows of 128 to 2048 bytes with up to 36 KiB per pair 2-10 % faster
+// (512-byte rows x 24 row-blocks 74.7 -> 70.8, the SWA move 67.7 -> 63.9);
+// whole pairs of 64 to 72 KiB (3 in flight per SM) the same or up to 12 %
+// slower, but split into chunks of at most 36 KiB 0.4-3 % faster (the decode
+// move's 128 KiB pairs in 4 chunks 353 -> 348); 64-byte rows 15 % slower.
+// So the launcher takes it for rows of at least 128 bytes, in chunks of at
+// most 36 KiB.
 #ifndef GTKV_MOVE_BULK
 #define GTKV_MOVE_BULK 1  // 0: every move takes the vector kernel
 #endif
@@ -105,10 +109,14 @@ __global__ void __launch_bounds__(kBlock) k_move(DevPool p, const int32_t* __res
 #ifndef GTKV_MOVE_BULK_MIN_ROW
 #define GTKV_MOVE_BULK_MIN_ROW 128
 #endif
+#ifndef GTKV_MOVE_BULK_SPLIT
+#define GTKV_MOVE_BULK_SPLIT 1  // 0: pairs over GTKV_MOVE_BULK_MAX_BYTES keep the vector kernel
+#endif
 
 __global__ void __launch_bounds__(32) k_move_bulk(DevPool p, const int32_t* __restrict__ src_ids,
-                                                  const int32_t* __restrict__ dst_ids, int64_t n) {
-  extern __shared__ __align__(128) uint4 sbuf[];  // the pair's 2L rows (L for MLA), block order
+                                                  const int32_t* __restrict__ dst_ids, int64_t n, int chunks,
+                                                  int chunk_rows) {
+  extern __shared__ __align__(128) uint4 sbuf[];  // one chunk of the pair's row-blocks, in block order
   __shared__ __align__(8) uint64_t bar;
   const int lane = threadIdx.x;
   const int64_t vpr = p.vpr;
@@ -118,17 +126,22 @@ __global__ void __launch_bounds__(32) k_move_bulk(DevPool p, const int32_t* __re
   if (lane == 0) mbar_init(&bar);
   __syncwarp();
   uint32_t parity = 0;
-  for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+  const int64_t n_units = n * chunks;
+  for (int64_t w = blockIdx.x; w < n_units; w += gridDim.x) {
+    const int64_t i = w / chunks;
+    const int b0 = static_cast<int>(w - i * chunks) * chunk_rows;
+    const int b1 = b0 + chunk_rows < blocks ? b0 + chunk_rows : blocks;
     const int32_t s_id = __ldg(src_ids + i), d_id = __ldg(dst_ids + i);
     const int e = check_id(p, s_id) | check_id(p, d_id);
     if (e != 0) {
-      if (lane == 0) atomicOr(p.err, e);
+      if (lane == 0 && b0 == 0) atomicOr(p.err, e);
       continue;
     }
-    if (lane == 0) mbar_expect(&bar, rbytes * static_cast<uint32_t>(blocks));
+    if (lane == 0) mbar_expect(&bar, rbytes * static_cast<uint32_t>(b1 - b0));
     __syncwarp();  // the phase expects its bytes before any load can complete it
-    for (int b = lane; b < blocks; b += 32)
-      bulk_load(sbuf + b * vpr, p.base + (s_id + static_cast<int64_t>(b) * p.ps) * vpr, rbytes, &bar, pol.first);
+    for (int b = b0 + lane; b < b1; b += 32)
+      bulk_load(sbuf + (b - b0) * vpr, p.base + (s_id + static_cast<int64_t>(b) * p.ps) * vpr, rbytes, &bar,
+                pol.first);
     if (!__all_sync(kFull, mbar_wait_bounded(&bar, parity))) {
       if (lane == 0) atomicOr(p.err, KV_DEV_ERR_TIMEOUT);
       mbar_wait_bounded(&bar, parity);
@@ -136,10 +149,11 @@ __global__ void __launch_bounds__(32) k_move_bulk(DevPool p, const int32_t* __re
       return;
     }
     parity ^= 1;
-    for (int b = lane; b < blocks; b += 32)
-      bulk_store(p.base + (d_id + static_cast<int64_t>(b) * p.ps) * vpr, sbuf + b * vpr, rbytes, pol.first);
+    for (int b = b0 + lane; b < b1; b += 32)
+      bulk_store(p.base + (d_id + static_cast<int64_t>(b) * p.ps) * vpr, sbuf + (b - b0) * vpr, rbytes,
+                 pol.first);
     bulk_commit();
-    bulk_wait_read();  // the next pair's loads reuse the buffer
+    bulk_wait_read();  // the next unit's loads reuse the buffer
     __syncwarp();
   }
 }
@@ -150,12 +164,22 @@ cudaError_t launch_move(const DevPool& p, const int32_t* src, const int32_t* dst
                         cudaStream_t s) {
   const int64_t n_tasks = n * p.blocks;
   const int64_t pair_bytes = static_cast<int64_t>(p.blocks) * p.vpr * 16;
-  if (GTKV_MOVE_BULK && pair_bytes <= GTKV_MOVE_BULK_MAX_BYTES && p.vpr * 16 >= GTKV_MOVE_BULK_MIN_ROW) {
+  const int64_t R = p.vpr * 16;
+  if (GTKV_MOVE_BULK && R >= GTKV_MOVE_BULK_MIN_ROW &&
+      (pair_bytes <= GTKV_MOVE_BULK_MAX_BYTES || GTKV_MOVE_BULK_SPLIT)) {
     static_assert(GTKV_MOVE_BULK_MAX_BYTES <= 48 * 1024, "within the default dynamic shared memory limit");
-    const int smem = static_cast<int>(pair_bytes);
-    const unsigned grid = static_cast<unsigned>(n < 0x7fffffff ? n : 0x7fffffff);
-    k_move_bulk<<<grid, 32, smem, s>>>(p, src, dst, n);
-    return cudaGetLastError();
+    // a pair over GTKV_MOVE_BULK_MAX_BYTES is split into equal chunks of row-blocks, one block each
+    int64_t chunks = (pair_bytes + GTKV_MOVE_BULK_MAX_BYTES - 1) / GTKV_MOVE_BULK_MAX_BYTES;
+    if (chunks > p.blocks) chunks = p.blocks;
+    const int64_t chunk_rows = (p.blocks + chunks - 1) / chunks;
+    chunks = (p.blocks + chunk_rows - 1) / chunk_rows;
+    if (chunk_rows * R <= GTKV_MOVE_BULK_MAX_BYTES) {
+      const int smem = static_cast<int>(chunk_rows * R);
+      const int64_t units = n * chunks;
+      const unsigned grid = static_cast<unsigned>(units < 0x7fffffff ? units : 0x7fffffff);
+      k_move_bulk<<<grid, 32, smem, s>>>(p, src, dst, n, static_cast<int>(chunks), static_cast<int>(chunk_rows));
+      return cudaGetLastError();
+    }
   }
   return dispatch_row(p.vpr, [&]<int G, int VPL>() -> cudaError_t {
     constexpr int U0 = VPL == 0 ? 1 : (VPL >= GTKV_MOVE_VEC ? 1 : GTKV_MOVE_VEC / VPL);
