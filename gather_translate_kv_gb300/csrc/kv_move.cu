@@ -9,7 +9,7 @@
 // groups. Sources and destinations are disjoint by precondition, so loads use
 // the coherent path (the pool is written by this kernel) and need no ordering.
 // Rows of at least 128 bytes take the bulk-copy form below instead (one warp
-// per pair, or per chunk of at most 36 KiB of it, through shared memory).
+// per pair, or per chunk of at most 18 KiB of it, through shared memory).
 #include "kv_bulk.cuh"
 #include "kv_launch.h"
 #include "kv_tasks.cuh"
@@ -96,15 +96,16 @@ __global__ void __launch_bounds__(kBlock) k_move(DevPool p, const int32_t* __res
 // (us): rows of 128 to 2048 bytes with up to 36 KiB per pair 2-10 % faster
 // (512-byte rows x 24 row-blocks 74.7 -> 70.8, the SWA move 67.7 -> 63.9);
 // whole pairs of 64 to 72 KiB (3 in flight per SM) the same or up to 12 %
-// slower, but split into chunks of at most 36 KiB 0.4-3 % faster (the decode
-// move's 128 KiB pairs in 4 chunks 353 -> 348); 64-byte rows 15 % slower.
-// So the launcher takes it for rows of at least 128 bytes, in chunks of at
-// most 36 KiB.
+// slower, but split into chunks 0.4-3 % faster (the decode move 353 -> 348);
+// 64-byte rows 15 % slower. Chunks of 18 KiB against 36 KiB: the SWA move
+// 64.6 -> 62.8, the MLA move ~1 % faster, the rest within noise. So the
+// launcher takes this form for rows of at least 128 bytes, in chunks of at
+// most 18 KiB.
 #ifndef GTKV_MOVE_BULK
 #define GTKV_MOVE_BULK 1  // 0: every move takes the vector kernel
 #endif
 #ifndef GTKV_MOVE_BULK_MAX_BYTES
-#define GTKV_MOVE_BULK_MAX_BYTES 36864
+#define GTKV_MOVE_BULK_MAX_BYTES 18432  // bytes of a pair's rows per block (chunk)
 #endif
 #ifndef GTKV_MOVE_BULK_MIN_ROW
 #define GTKV_MOVE_BULK_MIN_ROW 128

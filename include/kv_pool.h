@@ -370,7 +370,7 @@ int kv_gather_plan_noalloc(const kv_pool_t* pool, const int32_t* block_table_dev
  * Device errors: an id outside [0, n_rows) sets KV_DEV_ERR_ROW and an id
  * whose offset id % (ps*2L) is >= ps sets KV_DEV_ERR_FORM; that pair is
  * skipped. With rows of at least 128 bytes a pair's 2L rows are copied
- * through shared memory by bulk copies, in chunks of at most 36 KiB, with a
+ * through shared memory by bulk copies, in chunks of at most 18 KiB, with a
  * bounded wait for the loads (KV_DEV_ERR_TIMEOUT); smaller rows are copied
  * row by row through registers. */
 int kv_move(const kv_pool_t* pool, const int32_t* src_ids_dev, const int32_t* dst_ids_dev, int64_t n,
